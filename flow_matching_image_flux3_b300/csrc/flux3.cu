@@ -1,0 +1,602 @@
+// flux3.cu -- libflux3.so: the C-ABI entry points of include/flux3.h.  Host-side
+// argument checks, TMA tensor-map encoding, workspace carving and kernel launches.
+// Every step of the block runs in the kernels of gemm.cuh, attention.cuh and simt.cuh.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/flux3.h"
+#include "sm103.cuh"
+#include "simt.cuh"
+#include "gemm.cuh"
+#include "attention.cuh"
+
+using namespace f3;
+
+namespace {
+
+constexpr int kMaxTokens = 1 << 22;
+
+// ------------------------------------------------------------------ driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool have_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// bf16 row-major [outer, inner] (row stride in bytes), box 64 x box_outer, 128-byte swizzle
+bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// bf16 [d2][d1][d0], strides in bytes, box 64 x 128 x 1, 128-byte swizzle
+bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2) {
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// ------------------------------------------------------------------ profiling marks
+struct Profiler {
+    bool on = false;
+    int cap = 0, n = 0;
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> kind;
+} g_prof;
+
+void prof_before(int kind, cudaStream_t st) {
+    if (!g_prof.on || g_prof.n >= g_prof.cap) return;
+    cudaEventRecord(g_prof.ev[2 * g_prof.n], st);
+    g_prof.kind[g_prof.n] = kind;
+}
+void prof_after(cudaStream_t st) {
+    if (!g_prof.on || g_prof.n >= g_prof.cap) return;
+    cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], st);
+    ++g_prof.n;
+}
+
+flux3_status launch_status() { return cudaGetLastError() == cudaSuccess ? FLUX3_OK : FLUX3_ERR_CUDA; }
+
+// ------------------------------------------------------------------ argument checks
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+size_t up256(size_t b) { return (b + 255) & ~size_t(255); }
+
+flux3_status check_dims(const flux3_dims* d) {
+    if (!d) return FLUX3_ERR_INVALID_ARG;
+    if (d->heads <= 0 || d->width <= 0 || d->ffn_hidden <= 0 || d->head_dim <= 0) return FLUX3_ERR_INVALID_ARG;
+    if (!(d->ln_eps > 0.f) || !(d->rms_eps > 0.f) || !(d->rope_theta > 0.f) || !std::isfinite(d->rope_theta))
+        return FLUX3_ERR_INVALID_ARG;
+    if ((long long)d->heads * d->head_dim != d->width) return FLUX3_ERR_INVALID_ARG;
+    if (d->head_dim != 128) return FLUX3_ERR_UNSUPPORTED;
+    if (d->heads % 2 != 0 || d->ffn_hidden % 128 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (d->width > 32 * 8 * kAdaLnMaxChunks) return FLUX3_ERR_UNSUPPORTED;
+    if (d->ffn_hidden > 65536) return FLUX3_ERR_UNSUPPORTED;
+    return FLUX3_OK;
+}
+
+flux3_status check_offsets(const int32_t* off, int n_seg, int n_tokens) {
+    if (!off || n_seg < 1 || n_seg > FLUX3_MAX_SEGMENTS) return FLUX3_ERR_INVALID_ARG;
+    if (off[0] != 0 || off[n_seg] != n_tokens) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < n_seg; ++i)
+        if (off[i + 1] < off[i]) return FLUX3_ERR_INVALID_ARG;
+    return FLUX3_OK;
+}
+
+flux3_status check_segs(const flux3_segments* s, int n_tokens, bool need_mod) {
+    if (!s) return FLUX3_ERR_INVALID_ARG;
+    flux3_status st = check_offsets(s->seg_off, s->n_seg, n_tokens);
+    if (st != FLUX3_OK) return st;
+    if (need_mod && (!s->mod || !al16(s->mod))) return FLUX3_ERR_INVALID_ARG;
+    return FLUX3_OK;
+}
+
+flux3_status check_weights(const flux3_block_weights* w, int n_w, bool in_proj, bool out_proj) {
+    if (!w || n_w < 1 || n_w > FLUX3_MAX_SEGMENTS) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < n_w; ++i) {
+        if (in_proj) {
+            if (!w[i].w_in || !al16(w[i].w_in) || !w[i].q_norm || !al16(w[i].q_norm) || !w[i].k_norm ||
+                !al16(w[i].k_norm) || (w[i].b_in && !al16(w[i].b_in)))
+                return FLUX3_ERR_INVALID_ARG;
+        }
+        if (out_proj) {
+            if (!w[i].w_out || !al16(w[i].w_out) || (w[i].b_out && !al16(w[i].b_out))) return FLUX3_ERR_INVALID_ARG;
+        }
+    }
+    return FLUX3_OK;
+}
+
+SegOffsets seg_table(const int32_t* off, int n_seg) {
+    SegOffsets t;
+    std::memset(&t, 0, sizeof t);
+    t.n_seg = n_seg;
+    for (int i = 0; i <= n_seg; ++i) t.off[i] = off[i];
+    return t;
+}
+
+// workspace carve-up of one block
+struct BlockWs {
+    __nv_bfloat16 *a, *q, *k, *vt, *y;
+    int ld_vt;
+    size_t bytes;
+};
+BlockWs block_ws_layout(const flux3_dims* d, int N, uint8_t* base) {
+    BlockWs w;
+    const size_t D = d->width, H = d->heads, F = d->ffn_hidden;
+    w.ld_vt = (N + 7) & ~7;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? base + off : nullptr;
+        off += up256(bytes);
+        return reinterpret_cast<__nv_bfloat16*>(p);
+    };
+    w.a = take((size_t)N * D * 2);
+    w.q = take(H * (size_t)N * 128 * 2);
+    w.k = take(H * (size_t)N * 128 * 2);
+    w.vt = take(H * 128 * (size_t)w.ld_vt * 2);
+    w.y = take((size_t)N * (D + F) * 2);
+    w.bytes = off;
+    return w;
+}
+
+// ------------------------------------------------------------------ launchers (checked args)
+flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& segs, const void* x, int n_rows, void* a,
+                       cudaStream_t st) {
+    if (n_rows == 0) return FLUX3_OK;
+    prof_before(FLUX3_KERNEL_ADALN, st);
+    adaln_kernel<<<(n_rows + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), n_rows, d->width, d->ln_eps, mod,
+                                                   segs, 0, static_cast<__nv_bfloat16*>(a));
+    prof_after(st);
+    return launch_status();
+}
+
+template <int BN, int EPI>
+flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
+    const int total = P.m_tiles * P.n_tiles;
+    if (total == 0) return FLUX3_OK;
+    const int smem = GemmCfg<BN>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return FLUX3_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return FLUX3_ERR_CUDA;
+    const int grid = total < sms ? total : sms;
+    prof_before(kind, st);
+    gemm_tcgen05_kernel<BN, EPI><<<grid, GEMM_THREADS, smem, st>>>(P);
+    prof_after(st);
+    return launch_status();
+}
+
+// groups of rows sharing one weight set; m-tiles never straddle a group
+void fill_groups(GemmParams& P, const int32_t* off, int n_seg, int n_w, int N) {
+    int tiles = 0;
+    if (n_w == 1) {
+        P.n_groups = 1;
+        P.grp[0] = {0, N, 0, 0};
+        tiles = (N + GEMM_BM - 1) / GEMM_BM;
+    } else {
+        P.n_groups = n_seg;
+        for (int s = 0; s < n_seg; ++s) {
+            P.grp[s] = {off[s], off[s + 1], tiles, s};
+            tiles += (off[s + 1] - off[s] + GEMM_BM - 1) / GEMM_BM;
+        }
+    }
+    P.m_tiles = tiles;
+}
+
+flux3_status run_in_proj(const flux3_dims* d, const flux3_block_weights* w, int n_w, const flux3_segments* segs, const void* a,
+                         int N, const float* rope, void* q, void* k, void* vt, int ld_vt, void* y, cudaStream_t st) {
+    if (N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    const int D = d->width, F = d->ffn_hidden, H = d->heads;
+    const int n_in = 3 * D + 2 * F;
+    if (!tmap_2d(&P.tm_a, a, D, N, (uint64_t)D * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < n_w; ++i) {
+        if (!tmap_2d(&P.tm_b[i], w[i].w_in, D, n_in, (uint64_t)D * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+        P.ew[i] = {w[i].b_in, w[i].q_norm, w[i].k_norm};
+    }
+    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N);
+    P.n_tiles = 3 * H / 2 + F / 128;
+    P.k_blocks = D / GEMM_BK;
+    P.heads = H; P.width = D; P.ffn = F; P.n_tokens = N; P.ld_vt = ld_vt; P.ld_y = D + F;
+    P.rms_eps = d->rms_eps;
+    P.rope = rope;
+    P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
+    P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
+    return launch_gemm<256, EPI_QKV_SWIGLU>(P, st, FLUX3_KERNEL_IN_PROJ);
+}
+
+flux3_status run_out_proj(const flux3_dims* d, const flux3_block_weights* w, int n_w, const flux3_segments* segs, const void* y,
+                          const void* x, void* x_out, int N, cudaStream_t st) {
+    if (N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    const int D = d->width, F = d->ffn_hidden;
+    const int K = D + F;
+    if (!tmap_2d(&P.tm_a, y, K, N, (uint64_t)K * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < n_w; ++i) {
+        if (!tmap_2d(&P.tm_b[i], w[i].w_out, K, D, (uint64_t)K * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+        P.ew[i] = {w[i].b_out, nullptr, nullptr};
+    }
+    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N);
+    P.n_tiles = D / 256;
+    P.k_blocks = K / GEMM_BK;
+    P.width = D;
+    P.x = static_cast<const __nv_bfloat16*>(x);
+    P.x_out = static_cast<__nv_bfloat16*>(x_out);
+    P.mod = segs->mod;
+    P.n_seg = segs->n_seg;
+    for (int i = 0; i <= segs->n_seg; ++i) P.seg_off[i] = segs->seg_off[i];
+    return launch_gemm<256, EPI_GATED_RESIDUAL>(P, st, FLUX3_KERNEL_OUT_PROJ);
+}
+
+flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const void* vt, int ld_vt, int N, const int32_t* off,
+                      int n_seg, void* out, int ld_out, bool f32, cudaStream_t st) {
+    if (N == 0) return FLUX3_OK;
+    const int H = d->heads;
+    if (f32) {
+        SegTable t;
+        std::memset(&t, 0, sizeof t);
+        t.n_seg = n_seg;
+        for (int i = 0; i <= n_seg; ++i) t.off[i] = off[i];
+        prof_before(FLUX3_KERNEL_ATTN_F32, st);
+        attn_f32_kernel<<<dim3((N + 3) / 4, H), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                                                             static_cast<const __nv_bfloat16*>(vt), ld_vt, N, t,
+                                                             static_cast<float*>(out), ld_out, 1.0f / sqrtf(128.f));
+        prof_after(st);
+        return launch_status();
+    }
+    AttnParams P;
+    std::memset(&P, 0, sizeof P);
+    if (!tmap_3d(&P.tm_q, q, 128, N, H, 256, (uint64_t)N * 256)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_3d(&P.tm_k, k, 128, N, H, 256, (uint64_t)N * 256)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_3d(&P.tm_v, vt, N, 128, H, (uint64_t)ld_vt * 2, (uint64_t)ld_vt * 256)) return FLUX3_ERR_INVALID_ARG;
+    P.n_tokens = N;
+    P.heads = H;
+    P.n_seg = n_seg;
+    int tiles = 0;
+    for (int s = 0; s < n_seg; ++s) {
+        P.seg_off[s] = off[s];
+        P.qt_begin[s] = tiles;
+        tiles += (off[s + 1] - off[s] + 127) / 128;
+    }
+    P.seg_off[n_seg] = off[n_seg];
+    P.qt_begin[n_seg] = tiles;
+    P.out = static_cast<__nv_bfloat16*>(out);
+    P.ld_out = ld_out;
+    P.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+    if (tiles == 0) return FLUX3_OK;
+    if (cudaFuncSetAttribute(attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_BYTES) != cudaSuccess)
+        return FLUX3_ERR_CUDA;
+    prof_before(FLUX3_KERNEL_ATTN, st);
+    attn_tcgen05_kernel<<<dim3(tiles, H), ATT_THREADS, ATT_SMEM_BYTES, st>>>(P);
+    prof_after(st);
+    return launch_status();
+}
+
+flux3_status run_block(const flux3_dims* d, const flux3_block_weights* w, int n_w, const flux3_segments* segs, const void* x,
+                       void* x_out, int N, const float* rope, void* ws, size_t ws_bytes, cudaStream_t st, bool stage1) {
+    flux3_status s = check_dims(d);
+    if (s != FLUX3_OK) return s;
+    if (N < 0 || N > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, N, true)) != FLUX3_OK) return s;
+    if ((s = check_weights(w, n_w, true, true)) != FLUX3_OK) return s;
+    if (N == 0) return FLUX3_OK;
+    if (!x || !x_out || !rope || !al16(x) || !al16(x_out) || !al16(rope)) return FLUX3_ERR_INVALID_ARG;
+    const BlockWs need = block_ws_layout(d, N, nullptr);
+    if (!ws || !al256(ws) || ws_bytes < need.bytes) return FLUX3_ERR_WORKSPACE;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    const BlockWs b = block_ws_layout(d, N, static_cast<uint8_t*>(ws));
+    const int D = d->width, F = d->ffn_hidden;
+    const SegOffsets so = seg_table(segs->seg_off, segs->n_seg);
+    if ((s = run_adaln(d, segs->mod, so, x, N, b.a, st)) != FLUX3_OK) return s;
+    if ((s = run_in_proj(d, w, n_w, segs, b.a, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK) return s;
+    const int32_t full[2] = {0, N};
+    if (stage1) s = run_attn(d, b.q, b.k, b.vt, b.ld_vt, N, segs->seg_off, segs->n_seg, b.y, D + F, false, st);
+    else s = run_attn(d, b.q, b.k, b.vt, b.ld_vt, N, full, 1, b.y, D + F, false, st);
+    if (s != FLUX3_OK) return s;
+    return run_out_proj(d, w, n_w, segs, b.y, x, x_out, N, st);
+}
+
+flux3_status run_final(const flux3_dims* d, const void* w_final, const float* b_final, int out_ch, const float* mod_final,
+                       const void* x, int n_rows, float* out, void* ws, size_t ws_bytes, cudaStream_t st) {
+    if (n_rows == 0) return FLUX3_OK;
+    const int D = d->width;
+    SegOffsets so;
+    std::memset(&so, 0, sizeof so);
+    so.n_seg = 1;
+    so.off[1] = n_rows;
+    flux3_status s = run_adaln(d, mod_final, so, x, n_rows, ws, st);
+    if (s != FLUX3_OK) return s;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    if (!tmap_2d(&P.tm_a, ws, D, n_rows, (uint64_t)D * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_2d(&P.tm_b[0], w_final, D, out_ch, (uint64_t)D * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    P.ew[0] = {b_final, nullptr, nullptr};
+    P.n_groups = 1;
+    P.grp[0] = {0, n_rows, 0, 0};
+    P.m_tiles = (n_rows + GEMM_BM - 1) / GEMM_BM;
+    P.n_tiles = out_ch / 128;
+    P.k_blocks = D / GEMM_BK;
+    P.width = D;
+    P.out = out;
+    P.ld_out = out_ch;
+    return launch_gemm<128, EPI_F32>(P, st, FLUX3_KERNEL_FINAL);
+}
+
+}  // namespace
+
+// ====================================================================== C-ABI
+extern "C" {
+
+const char* flux3_status_string(flux3_status s) {
+    switch (s) {
+        case FLUX3_OK: return "ok";
+        case FLUX3_ERR_INVALID_ARG: return "invalid argument";
+        case FLUX3_ERR_UNSUPPORTED: return "unsupported configuration";
+        case FLUX3_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case FLUX3_ERR_CUDA: return "CUDA error";
+        case FLUX3_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* flux3_version(void) { return "flux3-b300 0.1 (sm_103a, tcgen05)"; }
+
+flux3_status flux3_rope_build(const flux3_dims* dims, const int32_t* pos, int32_t n_tokens, float* rope, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!pos || !rope || !al16(pos) || !al16(rope)) return FLUX3_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const long long total = (long long)n_tokens * 64;
+    prof_before(FLUX3_KERNEL_ROPE, st);
+    rope_table_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(pos, n_tokens, std::log2((double)dims->rope_theta),
+                                                                       reinterpret_cast<float2*>(rope));
+    prof_after(st);
+    return launch_status();
+}
+
+flux3_status flux3_adaln_fwd(const flux3_dims* dims, const flux3_segments* segs, const void* x, int32_t n_tokens, void* a,
+                             flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, n_tokens, true)) != FLUX3_OK) return s;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!x || !a || !al16(x) || !al16(a) || x == a) return FLUX3_ERR_INVALID_ARG;
+    return run_adaln(dims, segs->mod, seg_table(segs->seg_off, segs->n_seg), x, n_tokens, a,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_in_proj_fwd(const flux3_dims* dims, const flux3_block_weights* w, int32_t n_w, const flux3_segments* segs,
+                               const void* a, int32_t n_tokens, const float* rope, void* q, void* k, void* vt, int32_t ld_vt,
+                               void* y, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, n_tokens, false)) != FLUX3_OK) return s;
+    if ((s = check_weights(w, n_w, true, false)) != FLUX3_OK) return s;
+    if (n_w != 1 && n_w != segs->n_seg) return FLUX3_ERR_INVALID_ARG;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!a || !rope || !q || !k || !vt || !y) return FLUX3_ERR_INVALID_ARG;
+    if (!al16(a) || !al16(rope) || !al16(q) || !al16(k) || !al16(vt) || !al16(y)) return FLUX3_ERR_INVALID_ARG;
+    if (ld_vt < n_tokens || ld_vt % 8 != 0) return FLUX3_ERR_INVALID_ARG;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    return run_in_proj(dims, w, n_w, segs, a, n_tokens, rope, q, k, vt, ld_vt, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_attn_fwd(const flux3_dims* dims, const void* q, const void* k, const void* vt, int32_t ld_vt, int32_t n_tokens,
+                            const int32_t* seg_off, int32_t n_seg, void* out, int32_t ld_out, int32_t fp32_debug,
+                            flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    const int32_t full[2] = {0, n_tokens};
+    if (!seg_off) {
+        if (n_seg != 1 && n_seg != 0) return FLUX3_ERR_INVALID_ARG;
+        seg_off = full;
+        n_seg = 1;
+    }
+    if ((s = check_offsets(seg_off, n_seg, n_tokens)) != FLUX3_OK) return s;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!q || !k || !vt || !out || !al16(q) || !al16(k) || !al16(vt) || !al16(out)) return FLUX3_ERR_INVALID_ARG;
+    if (ld_vt < n_tokens || ld_vt % 8 != 0) return FLUX3_ERR_INVALID_ARG;
+    if (ld_out < dims->width || ld_out % 8 != 0) return FLUX3_ERR_INVALID_ARG;
+    if (!fp32_debug && !have_encode()) return FLUX3_ERR_CUDA;
+    return run_attn(dims, q, k, vt, ld_vt, n_tokens, seg_off, n_seg, out, ld_out, fp32_debug != 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_out_proj_fwd(const flux3_dims* dims, const flux3_block_weights* w, int32_t n_w, const flux3_segments* segs,
+                                const void* y, const void* x, void* x_out, int32_t n_tokens, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, n_tokens, true)) != FLUX3_OK) return s;
+    if ((s = check_weights(w, n_w, false, true)) != FLUX3_OK) return s;
+    if (n_w != 1 && n_w != segs->n_seg) return FLUX3_ERR_INVALID_ARG;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!y || !x || !x_out || !al16(y) || !al16(x) || !al16(x_out)) return FLUX3_ERR_INVALID_ARG;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    return run_out_proj(dims, w, n_w, segs, y, x, x_out, n_tokens, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t flux3_block_workspace_size(const flux3_dims* dims, int32_t n_tokens) {
+    if (check_dims(dims) != FLUX3_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
+    return block_ws_layout(dims, n_tokens, nullptr).bytes;
+}
+
+flux3_status flux3_block_fwd(const flux3_dims* dims, const flux3_block_weights* w, const flux3_segments* segs, const void* x,
+                             void* x_out, int32_t n_tokens, const float* rope, void* ws, size_t ws_bytes, flux3_stream_t stream) {
+    return run_block(dims, w, 1, segs, x, x_out, n_tokens, rope, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+flux3_status flux3_stream_block_fwd(const flux3_dims* dims, const flux3_block_weights* w, const flux3_segments* segs,
+                                    const void* x, void* x_out, int32_t n_tokens, const float* rope, void* ws, size_t ws_bytes,
+                                    flux3_stream_t stream) {
+    if (!segs) return FLUX3_ERR_INVALID_ARG;
+    return run_block(dims, w, segs->n_seg, segs, x, x_out, n_tokens, rope, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream),
+                     true);
+}
+
+flux3_status flux3_final_fwd(const flux3_dims* dims, const void* w_final, const float* b_final, int32_t out_channels,
+                             const float* mod_final, const void* x, int32_t n_rows, float* out, void* ws, size_t ws_bytes,
+                             flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_rows < 0 || n_rows > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if (out_channels <= 0 || out_channels > 4096) return FLUX3_ERR_INVALID_ARG;
+    if (out_channels % 128 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (n_rows == 0) return FLUX3_OK;
+    if (!w_final || !mod_final || !x || !out || !al16(w_final) || !al16(mod_final) || !al16(x) || !al16(out) ||
+        (b_final && !al16(b_final)))
+        return FLUX3_ERR_INVALID_ARG;
+    if (!ws || !al256(ws) || ws_bytes < up256((size_t)n_rows * dims->width * 2)) return FLUX3_ERR_WORKSPACE;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    return run_final(dims, w_final, b_final, out_channels, mod_final, x, n_rows, out, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t flux3_dit_workspace_size(const flux3_dims* dims, int32_t n_img, int32_t n_ref, int32_t n_txt) {
+    if (check_dims(dims) != FLUX3_OK || n_img < 0 || n_ref < 0 || n_txt < 0) return 0;
+    const long long N = (long long)n_img + n_ref + n_txt;
+    if (N > kMaxTokens) return 0;
+    return up256((size_t)N * 128 * 4) + block_ws_layout(dims, (int)N, nullptr).bytes;
+}
+
+flux3_status flux3_dit_fwd(const flux3_dims* dims, const flux3_dit_weights* w, const flux3_dit_mod* mod, void* tokens,
+                           int32_t n_img, int32_t n_ref, int32_t n_txt, const int32_t* pos, float* velocity, void* ws,
+                           size_t ws_bytes, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (!w || !mod || n_img < 0 || n_ref < 0 || n_txt < 0) return FLUX3_ERR_INVALID_ARG;
+    const long long NN = (long long)n_img + n_ref + n_txt;
+    if (NN > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    const int N = (int)NN;
+    if (w->n_streams != (n_ref > 0 ? 3 : 2)) return FLUX3_ERR_INVALID_ARG;
+    if (w->n_stage1 < 0 || w->n_joint < 0 || (w->n_stage1 > 0 && (!w->stage1 || !mod->stage1)) ||
+        (w->n_joint > 0 && (!w->joint || !mod->joint)))
+        return FLUX3_ERR_INVALID_ARG;
+    if (w->out_channels <= 0 || w->out_channels > 4096) return FLUX3_ERR_INVALID_ARG;
+    if (w->out_channels % 128 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (N == 0) return FLUX3_OK;
+    if (!tokens || !pos || !velocity || !w->w_final || !mod->final) return FLUX3_ERR_INVALID_ARG;
+    if (!al16(tokens) || !al16(pos) || !al16(velocity)) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < w->n_stage1; ++i)
+        if ((s = check_weights(w->stage1 + (size_t)i * w->n_streams, w->n_streams, true, true)) != FLUX3_OK) return s;
+    for (int i = 0; i < w->n_joint; ++i)
+        if ((s = check_weights(w->joint + i, 1, true, true)) != FLUX3_OK) return s;
+    if (!ws || !al256(ws) || ws_bytes < flux3_dit_workspace_size(dims, n_img, n_ref, n_txt)) return FLUX3_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* rope = static_cast<float*>(ws);
+    uint8_t* bws = static_cast<uint8_t*>(ws) + up256((size_t)N * 128 * 4);
+    const size_t bws_bytes = ws_bytes - up256((size_t)N * 128 * 4);
+    if ((s = flux3_rope_build(dims, pos, N, rope, stream)) != FLUX3_OK) return s;
+    int32_t off[4] = {0, n_img, 0, 0};
+    int ns = w->n_streams;
+    if (ns == 3) {
+        off[2] = n_img + n_ref;
+        off[3] = N;
+    } else {
+        off[2] = N;
+    }
+    const size_t mstride = (size_t)ns * 3 * dims->width;
+    for (int b = 0; b < w->n_stage1; ++b) {
+        flux3_segments sg{ns, off, mod->stage1 + b * mstride};
+        if ((s = run_block(dims, w->stage1 + (size_t)b * ns, ns, &sg, tokens, tokens, N, rope, bws, bws_bytes, st, true)) !=
+            FLUX3_OK)
+            return s;
+    }
+    for (int b = 0; b < w->n_joint; ++b) {
+        flux3_segments sg{ns, off, mod->joint + b * mstride};
+        if ((s = run_block(dims, w->joint + b, 1, &sg, tokens, tokens, N, rope, bws, bws_bytes, st, false)) != FLUX3_OK) return s;
+    }
+    return run_final(dims, w->w_final, w->b_final, w->out_channels, mod->final, tokens, n_img, velocity, bws, bws_bytes, st);
+}
+
+flux3_status flux3_euler_step(float* latent, const float* velocity, int64_t n, float sigma, float sigma_next, flux3_stream_t stream) {
+    if (n < 0 || (n > 0 && (!latent || !velocity))) return FLUX3_ERR_INVALID_ARG;
+    if (n == 0) return FLUX3_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int sms = sm_count();
+    if (sms <= 0) return FLUX3_ERR_CUDA;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    prof_before(FLUX3_KERNEL_EULER, st);
+    euler_kernel<<<(unsigned)blocks, 256, 0, st>>>(latent, velocity, n, sigma_next - sigma);
+    prof_after(st);
+    return launch_status();
+}
+
+flux3_status flux3_device_error(uint32_t* flags, int32_t reset) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return FLUX3_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return FLUX3_ERR_CUDA;
+    if (reset) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &z, sizeof z) != cudaSuccess) return FLUX3_ERR_CUDA;
+    }
+    if (flags) *flags = v;
+    return v ? FLUX3_ERR_TIMEOUT : FLUX3_OK;
+}
+
+flux3_status flux3_profile_begin(int32_t capacity) {
+    if (capacity <= 0 || capacity > (1 << 16)) return FLUX3_ERR_INVALID_ARG;
+    for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+    g_prof.ev.assign(2 * (size_t)capacity, nullptr);
+    for (auto& e : g_prof.ev)
+        if (cudaEventCreate(&e) != cudaSuccess) return FLUX3_ERR_CUDA;
+    g_prof.kind.assign(capacity, 0);
+    g_prof.cap = capacity;
+    g_prof.n = 0;
+    g_prof.on = true;
+    return FLUX3_OK;
+}
+
+flux3_status flux3_profile_end(float* ms, int32_t* kinds, int32_t capacity, int32_t* n) {
+    if (!g_prof.on) return FLUX3_ERR_INVALID_ARG;
+    g_prof.on = false;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FLUX3_ERR_CUDA;
+    const int cnt = g_prof.n < capacity ? g_prof.n : capacity;
+    for (int i = 0; i < cnt; ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) return FLUX3_ERR_CUDA;
+        if (ms) ms[i] = t;
+        if (kinds) kinds[i] = g_prof.kind[i];
+    }
+    if (n) *n = cnt;
+    return FLUX3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,406 @@
+// gemm.cuh -- persistent tcgen05 GEMM, D = A B^T, bf16 in / fp32 accumulate in TMEM,
+// fed by TMA, with the block's fused epilogues:
+//   EPI_QKV_SWIGLU      input projection: per-head QK RMSNorm + 4-axis RoPE -> q, k;
+//                       v -> V^T; silu(gate) * up -> y[:, D:]  ("How it works":
+//                       attention and SwiGLU run in parallel on the same normalized input)
+//   EPI_GATED_RESIDUAL  output projection: x_out = x + gate_s * (acc + b_out)
+//   EPI_F32             plain fp32 store (+ bias): the output layer
+//
+// Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads, warp 1 issues
+// tcgen05.mma from one thread and owns the TMEM allocation, warps 2..5 run the
+// epilogue, one accumulator row (TMEM lane) per thread.  Two TMEM accumulators let
+// the epilogue of one tile overlap the MMAs of the next.
+#pragma once
+#include <cuda.h>
+#include "sm103.cuh"
+#include "../../include/flux3.h"
+
+namespace f3 {
+
+constexpr int GEMM_BM = 128;
+constexpr int GEMM_BK = 64;  // bf16 elements per 128-byte swizzle row
+constexpr int GEMM_THREADS = 192;
+
+enum EpiKind { EPI_QKV_SWIGLU = 0, EPI_GATED_RESIDUAL = 1, EPI_F32 = 2 };
+
+struct GemmGroup {
+    int row_begin, row_end, tile_begin, wset;
+};
+struct EpiWeights {
+    const float* bias;
+    const float* q_norm;
+    const float* k_norm;
+};
+
+struct GemmParams {
+    CUtensorMap tm_a;                      // A [rows, K]
+    CUtensorMap tm_b[FLUX3_MAX_SEGMENTS];  // B per weight set [rows, K]
+    EpiWeights ew[FLUX3_MAX_SEGMENTS];
+    GemmGroup grp[FLUX3_MAX_SEGMENTS];
+    int n_groups;
+    int m_tiles, n_tiles, k_blocks;
+    // EPI_QKV_SWIGLU
+    int heads, width, ffn, n_tokens, ld_vt, ld_y;
+    float rms_eps;
+    const float* rope;
+    __nv_bfloat16 *q, *k, *vt, *y;
+    // EPI_GATED_RESIDUAL
+    const __nv_bfloat16* x;
+    __nv_bfloat16* x_out;
+    const float* mod;
+    int n_seg;
+    int seg_off[FLUX3_MAX_SEGMENTS + 1];
+    // EPI_F32
+    float* out;
+    int ld_out;
+};
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
+    static constexpr int B_BYTES = BN * GEMM_BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+};
+
+F3_DEV int group_of_tile(const GemmParams& p, int mt) {
+    int g = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.n_groups; ++i)
+        if (mt >= p.grp[i].tile_begin) g = i;
+    return g;
+}
+
+// B rows of output tile n: two 128-row boxes.  For the input projection the SwiGLU
+// tiles pair gate rows (3D + 128 j ..) with up rows (3D + F + 128 j ..), so one
+// accumulator holds both halves of 128 outputs.
+template <int BN, int EPI>
+F3_DEV void b_rows(const GemmParams& p, int n, int& r0, int& r1) {
+    if (EPI == EPI_QKV_SWIGLU) {
+        const int nq = 3 * p.heads / 2;
+        if (n < nq) {
+            r0 = 256 * n;
+            r1 = r0 + 128;
+        } else {
+            const int j = n - nq;
+            r0 = 3 * p.width + 128 * j;
+            r1 = r0 + p.ffn;
+        }
+    } else {
+        r0 = BN * n;
+        r1 = r0 + 128;
+    }
+}
+
+F3_DEV void unpack32(const uint32_t (&r)[32], float* v) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// --------------------------------------------------------------------- epilogues
+F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
+    const int nq = 3 * p.heads / 2;
+    if (n < nq) {
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            const int hg = 2 * n + hh;  // head index in Q | K | V order
+            const int kind = hg / p.heads;
+            const int head = hg - kind * p.heads;
+            float v[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t t[32];
+                tmem_ld32(tacc + hh * 128 + c * 32, t);
+                tmem_ld_wait();
+                unpack32(t, v + c * 32);
+            }
+            if (!valid) continue;
+            if (w.bias) {
+                const float4* b4 = reinterpret_cast<const float4*>(w.bias + hg * 128);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float4 b = __ldg(b4 + i);
+                    v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
+                }
+            }
+            if (kind < 2) {
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 128; ++i) ss = fmaf(v[i], v[i], ss);
+                const float inv = rsqrtf(ss * (1.f / 128.f) + p.rms_eps);
+                const float4* g4 = reinterpret_cast<const float4*>(kind == 0 ? w.q_norm : w.k_norm);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float4 g = __ldg(g4 + i);
+                    v[4 * i] *= inv * g.x; v[4 * i + 1] *= inv * g.y; v[4 * i + 2] *= inv * g.z; v[4 * i + 3] *= inv * g.w;
+                }
+                const float4* cs = reinterpret_cast<const float4*>(p.rope + (size_t)r * 128);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {  // two pairs per float4: (cos0, sin0, cos1, sin1)
+                    const float4 c = __ldg(cs + i);
+                    const float a0 = v[4 * i], a1 = v[4 * i + 1], b0 = v[4 * i + 2], b1 = v[4 * i + 3];
+                    v[4 * i] = a0 * c.x - a1 * c.y;
+                    v[4 * i + 1] = a0 * c.y + a1 * c.x;
+                    v[4 * i + 2] = b0 * c.z - b1 * c.w;
+                    v[4 * i + 3] = b0 * c.w + b1 * c.z;
+                }
+                __nv_bfloat16* dst = (kind == 0 ? p.q : p.k) + ((size_t)head * p.n_tokens + r) * 128;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    st_global_v4(dst + 8 * i, pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                                 pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+            } else {
+                __nv_bfloat16* dst = p.vt + (size_t)head * 128 * p.ld_vt + r;
+#pragma unroll
+                for (int i = 0; i < 128; ++i) dst[(size_t)i * p.ld_vt] = __float2bfloat16_rn(v[i]);
+            }
+        }
+    } else {
+        const int j = n - nq;
+        __nv_bfloat16* dst = p.y + (size_t)r * p.ld_y + p.width + 128 * j;
+        const float* bg = w.bias ? w.bias + 3 * p.width + 128 * j : nullptr;
+        const float* bu = w.bias ? w.bias + 3 * p.width + p.ffn + 128 * j : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t tg[32], tu[32];
+            tmem_ld32(tacc + c * 32, tg);
+            tmem_ld32(tacc + 128 + c * 32, tu);
+            tmem_ld_wait();
+            if (!valid) continue;
+            float g[32], u[32];
+            unpack32(tg, g);
+            unpack32(tu, u);
+            if (bg) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) { g[i] += __ldg(bg + c * 32 + i); u[i] += __ldg(bu + c * 32 + i); }
+            }
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a0 = g[2 * i] / (1.f + __expf(-g[2 * i])) * u[2 * i];
+                const float a1 = g[2 * i + 1] / (1.f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+                o[i] = pack_bf16(a0, a1);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) st_global_v4(dst + c * 32 + 8 * i, o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+    }
+}
+
+template <int BN>
+F3_DEV void epi_gated_residual(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
+    int seg = 0;
+#pragma unroll 1
+    for (int s = 1; s < p.n_seg; ++s)
+        if (r >= p.seg_off[s]) seg = s;
+    const int D = p.width;
+    const float* gate = p.mod + ((size_t)seg * 3 + 2) * D;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t t[32];
+        tmem_ld32(tacc + c * 32, t);
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col = n * BN + c * 32;
+        float a[32];
+        unpack32(t, a);
+        if (w.bias) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
+        }
+        const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)r * D + col);
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 xv = *(xs + i);  // x may alias x_out: plain (coherent) load
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&xw[e]);
+                const int k = 8 * i + 2 * e;
+                const float g0 = __ldg(gate + col + k), g1 = __ldg(gate + col + k + 1);
+                o[4 * i + e] = pack_bf16(fmaf(g0, a[k], __bfloat162float(h.x)), fmaf(g1, a[k + 1], __bfloat162float(h.y)));
+            }
+        }
+        __nv_bfloat16* dst = p.x_out + (size_t)r * D + col;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_global_v4(dst + 8 * i, o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
+}
+
+template <int BN>
+F3_DEV void epi_f32(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t t[32];
+        tmem_ld32(tacc + c * 32, t);
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col = n * BN + c * 32;
+        float a[32];
+        unpack32(t, a);
+        if (w.bias) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
+        }
+        float* dst = p.out + (size_t)r * p.ld_out + col;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            st_global_v4(dst + 4 * i, __float_as_uint(a[4 * i]), __float_as_uint(a[4 * i + 1]), __float_as_uint(a[4 * i + 2]),
+                         __float_as_uint(a[4 * i + 3]));
+    }
+}
+
+// --------------------------------------------------------------------- the kernel
+template <int BN, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+    using C = GemmCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    const uint32_t smem_base = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tm_a);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const int total = p.m_tiles * p.n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const int n = t / p.m_tiles, mt = t - (t / p.m_tiles) * p.m_tiles;
+                const int g = group_of_tile(p, mt);
+                const int row0 = p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM;
+                const CUtensorMap* tb = &p.tm_b[p.grp[g].wset];
+                int r0, r1;
+                b_rows<BN, EPI>(p, n, r0, r1);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_BYTES;
+                    mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    tma_load_2d(sa, &p.tm_a, full_bar(s), kb * GEMM_BK, row0);
+                    tma_load_2d(sb, tb, full_bar(s), kb * GEMM_BK, r0);
+                    if (BN == 256) tma_load_2d(sb + 128 * 128, tb, full_bar(s), kb * GEMM_BK, r1);
+                    ++issued;
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let the copies already in flight land before the CTA exits
+                int back = issued < C::STAGES ? issued : C::STAGES;
+                int ss = s;
+                uint32_t pp = ph;
+                for (int i = 0; i < back; ++i) {
+                    if (--ss < 0) { ss = C::STAGES - 1; pp ^= 1u; }
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(full_bar(ss), pp) && globaltimer() - t0 < kWaitTimeoutNs) {}
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(full_bar(s), ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+                    const uint64_t ad = sdesc_kmajor_sw128(sa);
+                    const uint64_t bd = sdesc_kmajor_sw128(sa + C::A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < GEMM_BK / 16; ++k)
+                        mma_bf16_ss(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
+                    mma_commit(empty_bar(s));
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
+            }
+            // all issued MMAs retire before TMEM is released
+            mma_commit(drain_bar);
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < kWaitTimeoutNs) {}
+        }
+    } else {
+        // ---------------- epilogue warps 2..5
+        const int sub = warp & 3;  // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const int n = t / p.m_tiles, mt = t - (t / p.m_tiles) * p.m_tiles;
+            const int g = group_of_tile(p, mt);
+            const int row0 = p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM;
+            const int r = row0 + sub * 32 + lane;
+            const bool valid = r < p.grp[g].row_end;
+            if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16) + acc * BN;
+            const EpiWeights& w = p.ew[p.grp[g].wset];
+            if (EPI == EPI_QKV_SWIGLU) epi_qkv(p, w, n, tacc, valid ? r : 0, valid);
+            else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, n, tacc, valid ? r : 0, valid);
+            else epi_f32<BN>(p, w, n, tacc, valid ? r : 0, valid);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) { acc = 0; aph ^= 1u; }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace f3

@@ -1,0 +1,252 @@
+/*
+ * flux3.h -- C-ABI of libflux3.so: the FLUX.3 Image Klein transformer block on one
+ * B300 (sm_103a).
+ *
+ * What the block computes is stated on "Welcome FLUX.3 Image Klein in Diffusers",
+ * section "How it works": each block runs attention and a SwiGLU MLP in parallel on
+ * the same normalized input; scale, shift and gate come from timestep modulation set
+ * separately per stream (image at t, text and references at t = 0); RoPE uses four
+ * axes (t, h, w, l) of 32 head dims each; stage 1 runs 5 blocks per stream with the
+ * stream's own weights and self-only attention, stage 2 runs 28 shared blocks with
+ * full attention over the concatenated streams, and the output layers read the image
+ * tokens only.  The QK normalisation with a learned scale follows the module names
+ * "*.{query,key}_norm.scale" on the Miles page "FLUX 3 Image Klein", section 3
+ * ("Family config"), and the absence of a padding mask follows the same table
+ * (row "Micro-batch") and "How it works" (the transformer attends to the padding).
+ *
+ * Conventions for every entry point
+ *  - The caller owns all memory.  Pointers marked "device" must point to device
+ *    memory of the current CUDA device, 16-byte aligned; "host" pointers are read
+ *    during the call only.  The library allocates nothing.
+ *  - Work is enqueued on `stream` and runs asynchronously; the return value reports
+ *    argument validation and launch errors only.  No entry point synchronises the host
+ *    except flux3_device_error and flux3_profile_end.
+ *  - Arguments are checked on the host before anything is launched; a failed check
+ *    returns FLUX3_ERR_INVALID_ARG / FLUX3_ERR_UNSUPPORTED / FLUX3_ERR_WORKSPACE and
+ *    leaves every output untouched.  The library never traps or aborts.
+ *  - Activations are bf16 row-major; accumulation is fp32.  Batch is 1: one token
+ *    sequence per call, because the model takes no padding mask.
+ *  - Device kernels bound every wait; a wait that runs out sets a device flag that
+ *    flux3_device_error reports as FLUX3_ERR_TIMEOUT.
+ *  - Not thread-safe with respect to flux3_profile_begin / flux3_profile_end.
+ */
+#ifndef FLUX3_H
+#define FLUX3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. NULL is the legacy default stream. */
+typedef struct CUstream_st *flux3_stream_t;
+
+typedef enum flux3_status {
+    FLUX3_OK = 0,
+    FLUX3_ERR_INVALID_ARG = 1, /* NULL / misaligned pointer, bad size or offsets      */
+    FLUX3_ERR_UNSUPPORTED = 2, /* valid but not implemented (head_dim != 128, ...)     */
+    FLUX3_ERR_WORKSPACE = 3,   /* workspace pointer NULL/misaligned or too small       */
+    FLUX3_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed          */
+    FLUX3_ERR_TIMEOUT = 5      /* a device-side wait ran out (see flux3_device_error)  */
+} flux3_status;
+
+/* At most this many token segments (streams) per call. */
+#define FLUX3_MAX_SEGMENTS 16
+
+/* Model dimensions.  FLUX.3 Image Klein: width 3072, 24 heads x 128, SwiGLU hidden
+ * 9216 ("How it works" gives the width 3072 and the 128 head dims; the SGLang
+ * cookbook, section 4, the 24 heads).  Requirements: head_dim == 128 (else
+ * UNSUPPORTED), width == heads * head_dim, heads even, ffn_hidden % 128 == 0,
+ * eps > 0, rope_theta > 0.  Defaults used throughout: ln_eps = rms_eps = 1e-6,
+ * rope_theta = 10000. */
+typedef struct flux3_dims {
+    int32_t width;
+    int32_t heads;
+    int32_t head_dim;
+    int32_t ffn_hidden;
+    float ln_eps;     /* LayerNorm epsilon (no affine: the modulation replaces it)   */
+    float rms_eps;    /* QK RMSNorm epsilon                                          */
+    float rope_theta; /* RoPE base                                                    */
+} flux3_dims;
+
+/* One block's parameters (all device memory; nn.Linear layout, i.e. [out, in]).
+ *  w_in   bf16 [3D + 2F, D]: rows Q | K | V | gate | up, each head's 128 rows
+ *         contiguous ("How it works": attention and SwiGLU read the same normalized
+ *         input, so one projection produces both).
+ *  b_in   fp32 [3D + 2F] or NULL (zero).
+ *  q_norm, k_norm  fp32 [128]: learned RMSNorm scales ("*.query_norm.scale",
+ *         "*.key_norm.scale" on the Miles page, section 3).
+ *  w_out  bf16 [D, D + F]: columns attention-out | SwiGLU-out.
+ *  b_out  fp32 [D] or NULL (zero). */
+typedef struct flux3_block_weights {
+    const void *w_in;
+    const float *b_in;
+    const float *q_norm;
+    const float *k_norm;
+    const void *w_out;
+    const float *b_out;
+} flux3_block_weights;
+
+/* Token segments = streams, contiguous in token order [image | reference | text].
+ *  n_seg     1 .. FLUX3_MAX_SEGMENTS.
+ *  seg_off   HOST int32 [n_seg + 1], seg_off[0] = 0, non-decreasing, seg_off[n_seg] = N.
+ *  mod       DEVICE fp32 [n_seg][3][D]: (shift, scale, gate) of each stream.  The
+ *            image stream's vectors come from its timestep t and the text/reference
+ *            streams' from t = 0 ("How it works"); the library takes them as inputs. */
+typedef struct flux3_segments {
+    int32_t n_seg;
+    const int32_t *seg_off;
+    const float *mod;
+} flux3_segments;
+
+const char *flux3_status_string(flux3_status s);
+const char *flux3_version(void);
+
+/* ---- a1: RoPE table ("How it works": four axes t, h, w, l, 32 of the 128 dims each).
+ * pos   device int32 [N, 4]: (t, h, w, l) per token.
+ * rope  device fp32 [N, 64, 2]: (cos, sin) of pair p = 16 a + j (axis a, j = 0..15),
+ *       angle pos[a] * theta^(-2 j / 32), computed in fp64 and rounded to fp32.
+ *       Pair p rotates head dims (2p, 2p+1).  N == 0 is a no-op. */
+flux3_status flux3_rope_build(const flux3_dims *dims, const int32_t *pos, int32_t n_tokens,
+                              float *rope, flux3_stream_t stream);
+
+/* ---- a2 + a3: LayerNorm and per-stream modulation ("How it works": the block's
+ * normalized input; scale and shift per stream).
+ * a[r] = (x[r] - mean) * rsqrt(var + ln_eps) * (1 + scale_s) + shift_s, s = segment of r.
+ * x  device bf16 [N, D];  a  device bf16 [N, D] (may not alias x). */
+flux3_status flux3_adaln_fwd(const flux3_dims *dims, const flux3_segments *segs, const void *x,
+                             int32_t n_tokens, void *a, flux3_stream_t stream);
+
+/* ---- a4 .. a7: fused input projection with its epilogues.
+ * P = a W_in^T + b_in on tcgen05 tensor cores, then per token and head
+ *   q = RoPE(RMSNorm(P_q) * q_norm), k = RoPE(RMSNorm(P_k) * k_norm), v = P_v,
+ *   act = silu(P_gate) * P_up.
+ * w, n_w      host array of 1 weight set (shared by all tokens, stage 2) or of
+ *             segs->n_seg sets (segment s uses w[s], stage 1).
+ * a           device bf16 [N, D] (output of flux3_adaln_fwd).
+ * rope        device fp32 [N, 64, 2] (flux3_rope_build).
+ * q, k        device bf16 [H, N, 128].
+ * vt          device bf16 [H, 128, ld_vt]: V transposed (token index fastest),
+ *             ld_vt >= N and ld_vt % 8 == 0.
+ * y           device bf16 [N, D + F]: act is written to columns D .. D+F-1; columns
+ *             0 .. D-1 are left for the attention output. */
+flux3_status flux3_in_proj_fwd(const flux3_dims *dims, const flux3_block_weights *w, int32_t n_w,
+                               const flux3_segments *segs, const void *a, int32_t n_tokens,
+                               const float *rope, void *q, void *k, void *vt, int32_t ld_vt,
+                               void *y, flux3_stream_t stream);
+
+/* ---- a8: attention, softmax(q k^T / sqrt(128)) v per head, bidirectional, no padding
+ * mask ("How it works": the transformer attends to the text padding; stage 1 attends
+ * only within each stream, stage 2 over all tokens).
+ * seg_off     HOST int32 [n_seg + 1]: a query attends to the keys of its own segment.
+ *             n_seg = 1 (or seg_off = NULL) is full attention over the N tokens.
+ * q, k        device bf16 [H, N, 128];  vt  device bf16 [H, 128, ld_vt] (as above).
+ * out         device [N, ld_out], columns h*128 .. h*128+127 for head h; bf16, or
+ *             fp32 when fp32_debug != 0 (a SIMT fp32 path kept for checking; slow). */
+flux3_status flux3_attn_fwd(const flux3_dims *dims, const void *q, const void *k, const void *vt,
+                            int32_t ld_vt, int32_t n_tokens, const int32_t *seg_off, int32_t n_seg,
+                            void *out, int32_t ld_out, int32_t fp32_debug, flux3_stream_t stream);
+
+/* ---- a9: fused output projection with the gated residual ("How it works": gate from
+ * the stream's modulation).  x_out = x + gate_s * (y W_out^T + b_out).
+ * w, n_w   as for flux3_in_proj_fwd.   y  device bf16 [N, D + F].
+ * x        device bf16 [N, D];  x_out  device bf16 [N, D], may alias x. */
+flux3_status flux3_out_proj_fwd(const flux3_dims *dims, const flux3_block_weights *w, int32_t n_w,
+                                const flux3_segments *segs, const void *y, const void *x,
+                                void *x_out, int32_t n_tokens, flux3_stream_t stream);
+
+/* Workspace bytes for flux3_block_fwd / flux3_stream_block_fwd at N tokens. */
+size_t flux3_block_workspace_size(const flux3_dims *dims, int32_t n_tokens);
+
+/* ---- one stage-2 joint block ("How it works", "Stage 2": shared weights, full
+ * attention over [image | reference | text]).  Runs a2 .. a9 with one weight set.
+ * rope   device fp32 [N, 64, 2] from flux3_rope_build.
+ * ws     device workspace, 256-byte aligned, >= flux3_block_workspace_size bytes.
+ * x_out may alias x. */
+flux3_status flux3_block_fwd(const flux3_dims *dims, const flux3_block_weights *w,
+                             const flux3_segments *segs, const void *x, void *x_out,
+                             int32_t n_tokens, const float *rope, void *ws, size_t ws_bytes,
+                             flux3_stream_t stream);
+
+/* ---- one stage-1 block for every stream at once ("How it works", "Stage 1": each
+ * stream has its own weights and attends only to itself).  w is a host array of
+ * segs->n_seg weight sets; segment s uses w[s].  Other arguments as flux3_block_fwd. */
+flux3_status flux3_stream_block_fwd(const flux3_dims *dims, const flux3_block_weights *w,
+                                    const flux3_segments *segs, const void *x, void *x_out,
+                                    int32_t n_tokens, const float *rope, void *ws,
+                                    size_t ws_bytes, flux3_stream_t stream);
+
+/* ---- output layer on image tokens ("How it works": image tokens only go to the
+ * output layers).  out = ((LN(x) * (1 + scale) + shift) W_final^T + b_final), fp32.
+ * w_final    device bf16 [out_channels, D], out_channels % 128 == 0.
+ * b_final    device fp32 [out_channels] or NULL.
+ * mod_final  device fp32 [2][D]: shift, scale.
+ * x          device bf16 [n_rows, D];  out  device fp32 [n_rows, out_channels].
+ * ws         device workspace >= n_rows * D * 2 bytes (rounded up to 256). */
+flux3_status flux3_final_fwd(const flux3_dims *dims, const void *w_final, const float *b_final,
+                             int32_t out_channels, const float *mod_final, const void *x,
+                             int32_t n_rows, float *out, void *ws, size_t ws_bytes,
+                             flux3_stream_t stream);
+
+/* The denoiser stack's parameters (host structs pointing at device memory). */
+typedef struct flux3_dit_weights {
+    int32_t n_streams;                  /* 2 (image, text) or 3 (image, reference, text) */
+    int32_t n_stage1;                   /* blocks per stream before concatenation (5)   */
+    int32_t n_joint;                    /* shared joint blocks (28)                     */
+    const flux3_block_weights *stage1;  /* host [n_stage1][n_streams]                   */
+    const flux3_block_weights *joint;   /* host [n_joint]                               */
+    const void *w_final;                /* device bf16 [out_channels, D]                */
+    const float *b_final;               /* device fp32 [out_channels] or NULL           */
+    int32_t out_channels;               /* 128 (one packed latent patch)                */
+} flux3_dit_weights;
+
+/* Modulation vectors of every block (device fp32). */
+typedef struct flux3_dit_mod {
+    const float *stage1;  /* [n_stage1][n_streams][3][D] */
+    const float *joint;   /* [n_joint][n_streams][3][D]  */
+    const float *final;   /* [2][D]: shift, scale        */
+} flux3_dit_mod;
+
+size_t flux3_dit_workspace_size(const flux3_dims *dims, int32_t n_img, int32_t n_ref, int32_t n_txt);
+
+/* ---- the denoiser forward ("How it works": stage 1, concatenation, stage 2, output
+ * layers on image tokens).
+ * tokens    device bf16 [N, D], N = n_img + n_ref + n_txt, streams contiguous in the
+ *           order image | reference | text; overwritten with the last hidden state
+ *           (the concatenation of stage 1 is this buffer itself, no copy).
+ * pos       device int32 [N, 4].
+ * velocity  device fp32 [n_img, out_channels].
+ * n_ref == 0 requires n_streams == 2, n_ref > 0 requires n_streams == 3. */
+flux3_status flux3_dit_fwd(const flux3_dims *dims, const flux3_dit_weights *w,
+                           const flux3_dit_mod *mod, void *tokens, int32_t n_img, int32_t n_ref,
+                           int32_t n_txt, const int32_t *pos, float *velocity, void *ws,
+                           size_t ws_bytes, flux3_stream_t stream);
+
+/* ---- one Euler step of the flow ODE: latent += (sigma_next - sigma) * velocity.
+ * latent, velocity  device fp32 [n]. */
+flux3_status flux3_euler_step(float *latent, const float *velocity, int64_t n, float sigma,
+                              float sigma_next, flux3_stream_t stream);
+
+/* Synchronises the device and reads the device error flags (bit 0: a bounded wait ran
+ * out).  Returns FLUX3_ERR_TIMEOUT if any bit is set, else FLUX3_OK; flags may be NULL.
+ * reset != 0 clears the flags.  Blocking; not for the hot path. */
+flux3_status flux3_device_error(uint32_t *flags, int32_t reset);
+
+/* Kernel timing for measurement.  Between begin and end, every kernel launch is
+ * bracketed by two CUDA events on its stream (at most `capacity` launches are
+ * recorded).  flux3_profile_end synchronises, writes each launch's duration in ms and
+ * kind (FLUX3_KERNEL_*) into the host arrays and the count into *n. */
+enum {
+    FLUX3_KERNEL_ROPE = 1, FLUX3_KERNEL_ADALN = 2, FLUX3_KERNEL_IN_PROJ = 3,
+    FLUX3_KERNEL_ATTN = 4, FLUX3_KERNEL_OUT_PROJ = 5, FLUX3_KERNEL_FINAL = 6,
+    FLUX3_KERNEL_EULER = 7, FLUX3_KERNEL_ATTN_F32 = 8
+};
+flux3_status flux3_profile_begin(int32_t capacity);
+flux3_status flux3_profile_end(float *ms, int32_t *kinds, int32_t capacity, int32_t *n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLUX3_H */

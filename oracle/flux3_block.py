@@ -268,3 +268,67 @@ def dit_forward(x: np.ndarray, seg_off: Sequence[int], pos: np.ndarray,
 def euler_step(latent: np.ndarray, velocity: np.ndarray, sigma: float, sigma_next: float) -> np.ndarray:
     """One explicit Euler step of the flow ODE: x <- x + (sigma_next - sigma) * v."""
     return np.asarray(latent, dtype=F64) + (sigma_next - sigma) * np.asarray(velocity, dtype=F64)
+
+
+def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
+                       angles: np.ndarray, heads: int, rows: Sequence[int], head_dim: int = 128,
+                       ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
+                       rounding: Optional[str] = None) -> dict:
+    """The block's outputs for a few rows, at sizes where the whole block is too slow.
+
+    A row's output needs its own q, gate/up and the keys and values of every token it
+    attends to, so k and v are computed for all tokens of the attended ranges and q,
+    the attention, the SwiGLU output and x' only for `rows`.  Same steps and rounding
+    points as block_forward.  Returns k, v [N, H, d] and, per sampled row, q, attn,
+    act and x_out (arrays indexed like `rows`)."""
+    x = np.asarray(x, dtype=F64)
+    n, D = x.shape
+    H, d = heads, head_dim
+    nseg = len(seg_off) - 1
+    seg = segment_ids(seg_off)
+    F = (weights[0].w_in.shape[0] - 3 * D) // 2
+    a = _maybe_round(ada_ln(x, seg_off, mod, ln_eps), rounding)
+    if stage == 2:
+        ranges = [(0, n, weights[0])]
+    else:
+        ranges = [(seg_off[s], seg_off[s + 1], weights[s]) for s in range(nseg)]
+    k = np.empty((n, H, d)); v = np.empty((n, H, d))
+    for lo, hi, w in ranges:
+        pk = a[lo:hi] @ w.w_in[D:2 * D].T + w.b_in[D:2 * D]
+        pv = a[lo:hi] @ w.w_in[2 * D:3 * D].T + w.b_in[2 * D:3 * D]
+        k[lo:hi] = rope_rotate(rms_norm(pk.reshape(-1, H, d), w.k_norm, rms_eps), angles[lo:hi])
+        v[lo:hi] = pv.reshape(-1, H, d)
+    k = _maybe_round(k, rounding); v = _maybe_round(v, rounding)
+    rows = list(rows)
+    out = {"k": k, "v": v}
+    kh = np.ascontiguousarray(k.transpose(1, 0, 2))   # [H, N, d]
+    vh = np.ascontiguousarray(v.transpose(1, 0, 2))
+    scale = 1.0 / math.sqrt(d)
+    res = {key: [None] * len(rows) for key in ("q", "attn", "act", "x_out")}
+    # rows that share a weight set and an attended range are computed together
+    groups = {}
+    for i, r in enumerate(rows):
+        s = int(seg[r])
+        groups.setdefault(0 if stage == 2 else s, []).append(i)
+    for gkey, idx in groups.items():
+        w = weights[0] if stage == 2 else weights[gkey]
+        lo, hi = (0, n) if stage == 2 else (seg_off[gkey], seg_off[gkey + 1])
+        rr = [rows[i] for i in idx]
+        p = a[rr] @ w.w_in.T + w.b_in
+        q = rope_rotate(rms_norm(p[:, 0:D].reshape(-1, H, d), w.q_norm, rms_eps), angles[rr])
+        q = _maybe_round(q, rounding)
+        o = np.empty((len(rr), H, d))
+        for h in range(H):
+            sc = q[:, h] @ kh[h, lo:hi].T * scale
+            sc = sc - sc.max(axis=1, keepdims=True)
+            e = np.exp(sc)
+            o[:, h] = (e / e.sum(axis=1, keepdims=True)) @ vh[h, lo:hi]
+        o = _maybe_round(o.reshape(len(rr), -1), rounding)
+        act = _maybe_round(swiglu(p[:, 3 * D:3 * D + F], p[:, 3 * D + F:3 * D + 2 * F]), rounding)
+        y = np.concatenate([o, act], axis=1) @ w.w_out.T + w.b_out
+        xo = _maybe_round(x[rr] + mod[seg[rr], 2] * y, rounding)
+        for j, i in enumerate(idx):
+            res["q"][i], res["attn"][i], res["act"][i], res["x_out"][i] = q[j], o[j], act[j], xo[j]
+    for key in res:
+        out[key] = np.array(res[key])
+    return out

@@ -370,3 +370,21 @@ def test_synth_recipe_matches_page_facts():
     assert c.pos.shape == (144, 4)
     assert c.pos[:64, 3].abs().sum() == 0 and c.pos[64:, :3].abs().sum() == 0
     assert list(c.pos[64:, 3]) == list(range(80))
+
+
+@pytest.mark.parametrize("stage", [2, 1])
+def test_block_rows_match_full_block(stage):
+    case = _tiny_case(stage=stage, streams=[synth.Stream("image", 20, (4, 5)), synth.text_stream(9),
+                                            synth.Stream("ref", 6, (2, 3), t=1)])
+    full = _run(case, rounding="bf16")
+    w = [O.Weights(*(synth.as_f64(t) for t in (wi.w_in, wi.b_in, wi.q_norm, wi.k_norm, wi.w_out, wi.b_out)))
+         for wi in case.weights]
+    rows = [0, 7, 19, 20, 28, 29, 34]
+    r = O.block_forward_rows(synth.as_f64(case.x), w, case.seg_off, synth.as_f64(case.mod),
+                             O.rope_angles(case.pos.numpy(), 1e4), 2, rows, stage=stage, rounding="bf16")
+    np.testing.assert_allclose(r["x_out"], full.x_out[rows], rtol=0, atol=1e-2)
+    assert np.mean(r["x_out"] == full.x_out[rows]) > 0.97
+    np.testing.assert_allclose(r["k"], full.k, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["v"], full.v, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["q"], full.q[rows], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["act"], full.act[rows], rtol=0, atol=1e-2)
