@@ -13,6 +13,7 @@ data-parallel exchange); value = tokens of all ranks / max-over-ranks time.
 --impl reference times the CPU oracle on the host cores (rank 0 only).
 """
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -31,11 +32,10 @@ WORKLOAD = "FLUX.3 Image Klein stage-2 joint block, 1024x1024 image (4096 tok) +
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-rows", type=int, default=256, help="query rows per oracle sample")
     return p.parse_args()
 
 
@@ -57,15 +57,17 @@ def measured_peaks():
 
 
 class Clocks:
-    """nvidia-smi samples while the timed region runs."""
+    """nvidia-smi samples (every 100 ms) around the timed region; only the samples taken
+    between mark_start() and mark_end() are summarised."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
 
     def __enter__(self):
@@ -77,11 +79,18 @@ class Clocks:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.5)
         return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.2)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -92,24 +101,29 @@ class Clocks:
 
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm, mx, reasons = [], None, set()
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                if self.t0 and self.t1 and not (self.t0 <= ts <= self.t1):
+                    continue
+                sm.append(float(parts[2]))
+                mx = float(parts[3])
+                pw.append(float(parts[4]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
+            for nm, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(nm)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples in the timed region"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(pw)}
 
 
 def dist_setup(args):
@@ -119,32 +133,46 @@ def dist_setup(args):
     return ws, rank, local
 
 
-def cpu_oracle_sample(case, rows_per_sample, n_samples=1):
-    """Time the oracle on `rows_per_sample` query rows of the block (keys and values of
-    all 4,256 tokens included), on the host cores.  Returns (tokens/s, seconds, threads)."""
-    import numpy as np
-    import oracle as O
-    from flow_matching_image_flux3_b300 import synth
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        threads = os.cpu_count()
-    d = case.dims
-    w = [O.Weights(*(synth.as_f64(t) for t in (wi.w_in, wi.b_in, wi.q_norm, wi.k_norm, wi.w_out, wi.b_out)))
-         for wi in case.weights]
-    x, mod = synth.as_f64(case.x), synth.as_f64(case.mod)
-    ang = O.rope_angles(case.pos.numpy(), d.rope_theta)
-    times = []
-    for s in range(n_samples):
-        r0 = (s * rows_per_sample) % case.n
-        rows = list(range(r0, min(r0 + rows_per_sample, case.n)))
+class OracleSampler:
+    """The CPU oracle on bounded samples of the 4,256-token block.
+
+    A sample of r query rows does r/N of the block's work: the keys and values of its
+    own rows (block_keys_values) and the rest of the block for those rows
+    (block_forward_rows), which attends over the keys and values of the whole sequence,
+    computed once before timing."""
+
+    def __init__(self, case):
+        import oracle as O
+        from flow_matching_image_flux3_b300 import synth
+        self.O, self.case = O, case
+        try:
+            from threadpoolctl import threadpool_info
+            self.threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        except Exception:
+            self.threads = os.cpu_count()
+        d = case.dims
+        self.w = [O.Weights(*(synth.as_f64(t) for t in (wi.w_in, wi.b_in, wi.q_norm, wi.k_norm, wi.w_out, wi.b_out)))
+                  for wi in case.weights]
+        self.x, self.mod = synth.as_f64(case.x), synth.as_f64(case.mod)
+        self.ang = O.rope_angles(case.pos.numpy(), d.rope_theta)
+        self.args = (self.x, self.w, case.seg_off, self.mod, self.ang, d.heads)
+        self.kv = O.block_keys_values(*self.args, stage=case.stage, rounding="bf16")
+        self.next_row = 0
+
+    def step(self, r):
+        n = self.case.n
+        rows = [(self.next_row + i) % n for i in range(r)]
+        self.next_row = (self.next_row + r) % n
         t0 = time.perf_counter()
-        O.block_forward_rows(x, w, case.seg_off, mod, ang, d.heads, rows, stage=case.stage, rounding="bf16")
-        times.append((time.perf_counter() - t0, len(rows)))
-    tot_t = sum(t for t, _ in times)
-    tot_r = sum(r for _, r in times)
-    return tot_r / tot_t, tot_t, threads, times
+        self.O.block_keys_values(*self.args, rows=rows, stage=self.case.stage, rounding="bf16")
+        self.O.block_forward_rows(*self.args, rows, stage=self.case.stage, rounding="bf16", kv=self.kv)
+        return time.perf_counter() - t0
+
+    def rows_for(self, seconds):
+        """Rows per sample so that one sample takes about `seconds`."""
+        t = self.step(32)
+        per_row = t / 32
+        return int(max(1, min(self.case.n, seconds / per_row)))
 
 
 def run_reference(args):
@@ -153,19 +181,21 @@ def run_reference(args):
         return
     from flow_matching_image_flux3_b300 import synth
     case = synth.config(1)
+    smp = OracleSampler(case)
+    # size each step so that warm-up + timed steps take about two minutes
+    r = smp.rows_for(120.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_oracle_sample(case, args.cpu_rows, 1)
-    rate, secs, threads, times = cpu_oracle_sample(case, args.cpu_rows, args.steps)
-    d = case.dims
-    g1, at, g2 = block_flops(d.width, d.ffn_hidden, case.n)
+        smp.step(r)
+    secs = sum(smp.step(r) for _ in range(args.steps))
+    rate = r * args.steps / secs
+    sample = (f"{r} query rows of the 4256-token block per step: their keys/values and the rest of the block "
+              f"for them, attending over keys/values of all 4256 tokens computed once before timing; fp64 NumPy")
     out = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": case.n, "sample": f"{args.cpu_rows} query rows per step"},
-        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{args.cpu_rows} consecutive query rows of the 4256-token block per step "
-                                   f"(keys/values of all 4256 tokens computed each step), fp64 NumPy"},
+        "config": {"workload": WORKLOAD, "tokens": case.n, "rows_per_step": r},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": smp.threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -220,11 +250,13 @@ def run_ours(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         barrier()
+        clk.mark_start()
         ev0.record(stream)
         for _ in range(args.steps):
             step(x, x_out)
         ev1.record(stream)
         barrier()
+        clk.mark_end()
     ms = ev0.elapsed_time(ev1)
     if ws > 1:
         t = torch.tensor([ms], device=dev)
@@ -252,21 +284,42 @@ def run_ours(args):
     achieved = g1 / (gemm1_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
 
-    # ---- end to end through the C-ABI with host buffers: H2D x, block, D2H x_out
-    x_host = case.x.pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-    x_dev2 = torch.empty_like(x)
-    for _ in range(3):
-        x_dev2.copy_(x_host, non_blocking=True)
-        step(x_dev2, x_out)
-        out_host.copy_(x_out, non_blocking=True)
+    # ---- end to end through the C-ABI with host buffers: every step copies its input
+    # from pinned host memory (H2D) and its result back (D2H).  Copies run on their own
+    # streams, double-buffered, so step i's compute overlaps step i+1's upload and step
+    # i-1's download.
+    x_host = [case.x.pin_memory() for _ in range(2)]
+    out_host = [torch.empty_like(case.x).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    o_dev = [torch.empty_like(x) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(computed[b])          # x_dev[b] no longer read by step i-2
+                x_dev[b].copy_(x_host[b], non_blocking=True)
+                uploaded[b].record(h2d)
+            stream.wait_event(uploaded[b])
+            stream.wait_event(downloaded[b])         # o_dev[b] already copied out (step i-2)
+            step(x_dev[b], o_dev[b])
+            computed[b].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(computed[b])
+                out_host[b].copy_(o_dev[b], non_blocking=True)
+                downloaded[b].record(d2h)
+        stream.wait_event(downloaded[0])
+        stream.wait_event(downloaded[1])
+
+    e2e(4)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        x_dev2.copy_(x_host, non_blocking=True)
-        step(x_dev2, x_out)
-        out_host.copy_(x_out, non_blocking=True)
+    e2e(args.steps)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
@@ -274,14 +327,18 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    assert torch.equal(out_host[(args.steps - 1) & 1], x_out.cpu()), "end-to-end output differs"
     assert B.device_error() == 0
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, secs, threads, _ = cpu_oracle_sample(case, args.cpu_rows, 4)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"4 x {args.cpu_rows} query rows of the 4256-token block (keys/values of all tokens "
-                         f"computed each time), fp64 NumPy, {secs:.1f} s"}
+        smp = OracleSampler(case)
+        r = smp.rows_for(2.0)
+        secs = sum(smp.step(r) for _ in range(8))
+        cpu = {"value": 8 * r / secs, "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
+               "sample": f"8 samples x {r} query rows of the 4256-token block ({secs:.1f} s): each sample computes "
+                         f"its rows' keys/values and the rest of the block for them, attending over keys/values "
+                         f"of all tokens computed once before timing; fp64 NumPy"}
 
     if rank == 0:
         out = {
@@ -298,7 +355,8 @@ def run_ours(args):
                          "peak_source": f"{peaks['source']} bf16 burst", "traffic": None},
             "kernels": kern,
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+                    "h2d_bytes_per_step": x_host[0].numel() * 2, "d2h_bytes_per_step": out_host[0].numel() * 2,
+                    "ms_per_step": e2e_ms / args.steps, "copies": "pinned host, overlapped with compute"},
             "gpu_launches": 5 * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

@@ -286,6 +286,8 @@ class DitArgs:
     def __init__(self, stage1: Sequence[Sequence], joint: Sequence, w_final: torch.Tensor,
                  b_final: Optional[torch.Tensor], mod_stage1: Optional[torch.Tensor], mod_joint: Optional[torch.Tensor],
                  mod_final: torch.Tensor, n_streams: int):
+        # the structs hold raw device addresses: keep every tensor alive with this object
+        self._keep = [stage1, joint, w_final, b_final, mod_stage1, mod_joint, mod_final]
         flat = [w for blk in stage1 for w in blk]
         self.s1 = _weights_array(flat) if flat else None
         self.j = _weights_array(joint) if joint else None

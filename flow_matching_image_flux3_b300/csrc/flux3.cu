@@ -173,8 +173,9 @@ flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& 
                        cudaStream_t st) {
     if (n_rows == 0) return FLUX3_OK;
     prof_before(FLUX3_KERNEL_ADALN, st);
-    adaln_kernel<<<(n_rows + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), n_rows, d->width, d->ln_eps, mod,
-                                                   segs, 0, static_cast<__nv_bfloat16*>(a));
+    if (!launch_adaln(d->width, static_cast<const __nv_bfloat16*>(x), n_rows, d->ln_eps, mod, segs,
+                      static_cast<__nv_bfloat16*>(a), st))
+        return FLUX3_ERR_UNSUPPORTED;
     prof_after(st);
     return launch_status();
 }
@@ -381,8 +382,9 @@ flux3_status flux3_rope_build(const flux3_dims* dims, const int32_t* pos, int32_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const long long total = (long long)n_tokens * 64;
     prof_before(FLUX3_KERNEL_ROPE, st);
-    rope_table_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(pos, n_tokens, std::log2((double)dims->rope_theta),
-                                                                       reinterpret_cast<float2*>(rope));
+    RopeFreqs fr;
+    for (int j = 0; j < 16; ++j) fr.f[j] = std::pow((double)dims->rope_theta, -(double)(2 * j) / 32.0);
+    rope_table_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(pos, n_tokens, fr, reinterpret_cast<float2*>(rope));
     prof_after(st);
     return launch_status();
 }

@@ -270,35 +270,50 @@ def euler_step(latent: np.ndarray, velocity: np.ndarray, sigma: float, sigma_nex
     return np.asarray(latent, dtype=F64) + (sigma_next - sigma) * np.asarray(velocity, dtype=F64)
 
 
-def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
-                       angles: np.ndarray, heads: int, rows: Sequence[int], head_dim: int = 128,
-                       ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
-                       rounding: Optional[str] = None) -> dict:
-    """The block's outputs for a few rows, at sizes where the whole block is too slow.
-
-    A row's output needs its own q, gate/up and the keys and values of every token it
-    attends to, so k and v are computed for all tokens of the attended ranges and q,
-    the attention, the SwiGLU output and x' only for `rows`.  Same steps and rounding
-    points as block_forward.  Returns k, v [N, H, d] and, per sampled row, q, attn,
-    act and x_out (arrays indexed like `rows`)."""
+def block_keys_values(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
+                      angles: np.ndarray, heads: int, rows: Optional[Sequence[int]] = None, head_dim: int = 128,
+                      ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
+                      rounding: Optional[str] = None):
+    """Keys and values [len(rows), H, d] of the given rows (all rows by default): the
+    same steps as block_forward up to k and v, row by row."""
     x = np.asarray(x, dtype=F64)
     n, D = x.shape
     H, d = heads, head_dim
-    nseg = len(seg_off) - 1
+    seg = segment_ids(seg_off)
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    a = _maybe_round(modulate(layer_norm(x[rows], ln_eps), mod[seg[rows], 0], mod[seg[rows], 1]), rounding)
+    k = np.empty((len(rows), H, d)); v = np.empty((len(rows), H, d))
+    wsel = np.zeros(len(rows), dtype=np.int64) if stage == 2 else seg[rows]
+    for wi in np.unique(wsel):
+        m = wsel == wi
+        w = weights[wi]
+        pk = a[m] @ w.w_in[D:2 * D].T + w.b_in[D:2 * D]
+        pv = a[m] @ w.w_in[2 * D:3 * D].T + w.b_in[2 * D:3 * D]
+        k[m] = rope_rotate(rms_norm(pk.reshape(-1, H, d), w.k_norm, rms_eps), angles[rows[m]])
+        v[m] = pv.reshape(-1, H, d)
+    return _maybe_round(k, rounding), _maybe_round(v, rounding)
+
+
+def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
+                       angles: np.ndarray, heads: int, rows: Sequence[int], head_dim: int = 128,
+                       ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
+                       rounding: Optional[str] = None, kv=None) -> dict:
+    """The block's outputs for a few rows, at sizes where the whole block is too slow.
+
+    A row's output needs its own q, gate/up and the keys and values of every token it
+    attends to, so k and v are computed for all tokens (unless given as kv = (k, v) from
+    block_keys_values) and q, the attention, the SwiGLU output and x' only for `rows`.
+    Same steps and rounding points as block_forward.  Returns k, v [N, H, d] and, per
+    sampled row, q, attn, act and x_out (arrays indexed like `rows`)."""
+    x = np.asarray(x, dtype=F64)
+    n, D = x.shape
+    H, d = heads, head_dim
     seg = segment_ids(seg_off)
     F = (weights[0].w_in.shape[0] - 3 * D) // 2
-    a = _maybe_round(ada_ln(x, seg_off, mod, ln_eps), rounding)
-    if stage == 2:
-        ranges = [(0, n, weights[0])]
-    else:
-        ranges = [(seg_off[s], seg_off[s + 1], weights[s]) for s in range(nseg)]
-    k = np.empty((n, H, d)); v = np.empty((n, H, d))
-    for lo, hi, w in ranges:
-        pk = a[lo:hi] @ w.w_in[D:2 * D].T + w.b_in[D:2 * D]
-        pv = a[lo:hi] @ w.w_in[2 * D:3 * D].T + w.b_in[2 * D:3 * D]
-        k[lo:hi] = rope_rotate(rms_norm(pk.reshape(-1, H, d), w.k_norm, rms_eps), angles[lo:hi])
-        v[lo:hi] = pv.reshape(-1, H, d)
-    k = _maybe_round(k, rounding); v = _maybe_round(v, rounding)
+    if kv is None:
+        kv = block_keys_values(x, weights, seg_off, mod, angles, heads, None, head_dim, ln_eps, rms_eps, stage,
+                               rounding)
+    k, v = kv
     rows = list(rows)
     out = {"k": k, "v": v}
     kh = np.ascontiguousarray(k.transpose(1, 0, 2))   # [H, N, d]
@@ -313,8 +328,9 @@ def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[
     for gkey, idx in groups.items():
         w = weights[0] if stage == 2 else weights[gkey]
         lo, hi = (0, n) if stage == 2 else (seg_off[gkey], seg_off[gkey + 1])
-        rr = [rows[i] for i in idx]
-        p = a[rr] @ w.w_in.T + w.b_in
+        rr = np.array([rows[i] for i in idx])
+        a = _maybe_round(modulate(layer_norm(x[rr], ln_eps), mod[seg[rr], 0], mod[seg[rr], 1]), rounding)
+        p = a @ w.w_in.T + w.b_in
         q = rope_rotate(rms_norm(p[:, 0:D].reshape(-1, H, d), w.q_norm, rms_eps), angles[rr])
         q = _maybe_round(q, rounding)
         o = np.empty((len(rr), H, d))

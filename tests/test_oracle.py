@@ -388,3 +388,17 @@ def test_block_rows_match_full_block(stage):
     np.testing.assert_allclose(r["v"], full.v, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(r["q"], full.q[rows], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(r["act"], full.act[rows], rtol=0, atol=1e-2)
+
+
+def test_block_keys_values_of_some_rows_match_all_rows():
+    case = _tiny_case(stage=1, streams=[synth.Stream("image", 20, (4, 5)), synth.text_stream(9)])
+    w = [O.Weights(*(synth.as_f64(t) for t in (wi.w_in, wi.b_in, wi.q_norm, wi.k_norm, wi.w_out, wi.b_out)))
+         for wi in case.weights]
+    args = (synth.as_f64(case.x), w, case.seg_off, synth.as_f64(case.mod), O.rope_angles(case.pos.numpy(), 1e4), 2)
+    k, v = O.block_keys_values(*args, stage=1)
+    rows = [3, 19, 20, 28]
+    k2, v2 = O.block_keys_values(*args, rows=rows, stage=1)
+    np.testing.assert_allclose(k2, k[rows], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(v2, v[rows], rtol=1e-13, atol=1e-13)
+    full = _run(case)
+    np.testing.assert_allclose(k, full.k, rtol=1e-12, atol=1e-12)
