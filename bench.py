@@ -46,6 +46,22 @@ def block_flops(D, F, n):
     return gemm1, attn, gemm2
 
 
+# DRAM traffic of one in_proj launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
+# ncu capture summarised in profiles/joint_block_4256_ncu_full.md; reported only while the
+# kernel sources are the ones that capture measured.
+IN_PROJ_TRAFFIC_BYTES = (199.0 + 138.1) * 1e6
+IN_PROJ_SOURCES = {"gemm.cuh": "d175a4c52a776cf1", "sm103.cuh": "93930c071c5bf73e"}
+
+
+def in_proj_traffic():
+    import hashlib
+    for name, digest in IN_PROJ_SOURCES.items():
+        path = os.path.join(ROOT, "flow_matching_image_flux3_b300", "csrc", name)
+        if hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] != digest:
+            return None
+    return IN_PROJ_TRAFFIC_BYTES
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -282,7 +298,11 @@ def run_ours(args):
             kern[k]["tflops"] = f / (kern[k]["avg_ms"] / 1e3) / 1e12
     gemm1_ms = kern["in_proj"]["avg_ms"]
     achieved = g1 / (gemm1_ms / 1e3) / 1e12
-    peak = peaks["bf16_tflops"]
+    # a timed loop longer than half a second runs under the power cap: compare with the
+    # sustained cuBLAS figure; shorter runs with the burst figure
+    long_loop = sec > 0.5
+    peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
+    peak_src = f"{peaks['source']} bf16 {'sustained' if long_loop else 'burst'}"
 
     # ---- end to end through the C-ABI with host buffers: every step copies its input
     # from pinned host memory (H2D) and its result back (D2H).  Copies run on their own
@@ -347,12 +367,14 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "tflops": flops * args.steps * ws / sec / 1e12,
             "pct_of_peak": 100.0 * (flops * args.steps / sec / 1e12) / peak,
+            "pct_of_burst_peak": 100.0 * (flops * args.steps / sec / 1e12) / peaks["bf16_tflops"],
             "config": {"workload": WORKLOAD, "tokens": N, "global_batch": ws, "seq_len": N,
                        "parallelism": f"replicas x{ws}", "l2": "inputs exceed L2 (weights 245 MB per step)",
                        "flops_per_step": flops},
             "roofline": {"bound": "tensor", "kernel": "in_proj (fused input projection GEMM)",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peaks['source']} bf16 burst", "traffic": None},
+                         "peak_source": peak_src, "traffic": in_proj_traffic(),
+                         "algorithmic_flops_per_launch": g1},
             "kernels": kern,
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": x_host[0].numel() * 2, "d2h_bytes_per_step": out_host[0].numel() * 2,
