@@ -78,6 +78,8 @@ def _load() -> ctypes.CDLL:
         "flux3_dit_fwd": (c_i32, [P(flux3_dims), P(flux3_dit_weights), P(flux3_dit_mod), c_vp, c_i32, c_i32, c_i32,
                                   c_vp, c_vp, c_vp, c_size, c_vp]),
         "flux3_euler_step": (c_i32, [c_vp, c_vp, ctypes.c_int64, c_f32, c_f32, c_vp]),
+        "flux3_block_fwd_static": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp,
+                                           c_i32, c_vp, c_vp]),
         "flux3_device_error": (c_i32, [P(ctypes.c_uint32), c_i32]),
         "flux3_profile_begin": (c_i32, [c_i32]),
         "flux3_profile_end": (c_i32, [P(c_f32), P(c_i32), c_i32, P(c_i32)]),
@@ -94,8 +96,9 @@ EXPORTED = [
     "flux3_status_string", "flux3_version", "flux3_rope_build", "flux3_adaln_fwd", "flux3_in_proj_fwd",
     "flux3_attn_fwd", "flux3_out_proj_fwd", "flux3_block_workspace_size", "flux3_block_fwd",
     "flux3_stream_block_fwd", "flux3_final_fwd", "flux3_dit_workspace_size", "flux3_dit_fwd", "flux3_euler_step",
-    "flux3_device_error", "flux3_profile_begin", "flux3_profile_end",
+    "flux3_device_error", "flux3_profile_begin", "flux3_profile_end", "flux3_block_fwd_static",
 ]
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 def _check(fn: str, st: int) -> None:
@@ -243,6 +246,20 @@ def block_fwd(dims, weights, seg_off: Sequence[int], mod: torch.Tensor, x: torch
     _check("flux3_block_fwd", lib.flux3_block_fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(s.s),
                                                   _ptr(x, torch.bfloat16), _ptr(x_out, torch.bfloat16), n,
                                                   _ptr(rope, torch.float32), _ptr(ws), ws.numel(), _stream(stream)))
+    return x_out
+
+
+def block_fwd_static(dims, weights, seg_off: Sequence[int], mod: torch.Tensor, x: torch.Tensor, rope: torch.Tensor,
+                     x_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """block_fwd for callers that cannot allocate device memory: the scratch is the
+    library's own static device array (at most STATIC_SCRATCH_BYTES), so no workspace is
+    passed.  Calls share that array; do not overlap them on the GPU."""
+    x_out = x_out if x_out is not None else torch.empty_like(x)
+    d, s = make_dims(dims), Segments(seg_off, mod)
+    w = block_weights(weights)
+    _check("flux3_block_fwd_static", lib.flux3_block_fwd_static(ctypes.byref(d), ctypes.byref(w), ctypes.byref(s.s),
+                                                                _ptr(x, torch.bfloat16), _ptr(x_out, torch.bfloat16),
+                                                                x.shape[0], _ptr(rope, torch.float32), _stream(stream)))
     return x_out
 
 

@@ -356,6 +356,31 @@ flux3_status run_final(const flux3_dims* d, const void* w_final, const float* b_
 
 }  // namespace
 
+// ---------------------------------------------------------------- static scratch
+// Scratch for flux3_block_fwd_static: one file-scope device array.  Host code may not use
+// the symbol as an address; the device address is looked up once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[FLUX3_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+flux3_status static_scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FLUX3_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FLUX3_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FLUX3_ERR_CUDA;
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return FLUX3_OK;
+}
+}  // namespace
+
 // ====================================================================== C-ABI
 extern "C" {
 
@@ -545,6 +570,18 @@ flux3_status flux3_dit_fwd(const flux3_dims* dims, const flux3_dit_weights* w, c
         if ((s = run_block(dims, w->joint + b, 1, &sg, tokens, tokens, N, rope, bws, bws_bytes, st, false)) != FLUX3_OK) return s;
     }
     return run_final(dims, w->w_final, w->b_final, w->out_channels, mod->final, tokens, n_img, velocity, bws, bws_bytes, st);
+}
+
+flux3_status flux3_block_fwd_static(const flux3_dims* dims, const flux3_block_weights* w, const flux3_segments* segs,
+                                    const void* x, void* x_out, int32_t n_tokens, const float* rope, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if (block_ws_layout(dims, n_tokens, nullptr).bytes > FLUX3_STATIC_SCRATCH_BYTES) return FLUX3_ERR_WORKSPACE;
+    void* ws = nullptr;
+    if (n_tokens > 0 && (s = static_scratch_address(&ws)) != FLUX3_OK) return s;
+    return run_block(dims, w, 1, segs, x, x_out, n_tokens, rope, ws, FLUX3_STATIC_SCRATCH_BYTES,
+                     reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 flux3_status flux3_euler_step(float* latent, const float* velocity, int64_t n, float sigma, float sigma_next, flux3_stream_t stream) {

@@ -229,6 +229,31 @@ flux3_status flux3_dit_fwd(const flux3_dims *dims, const flux3_dit_weights *w,
 flux3_status flux3_euler_step(float *latent, const float *velocity, int64_t n, float sigma,
                               float sigma_next, flux3_stream_t stream);
 
+/* ---- flux3_block_fwd without a caller-provided workspace.
+ * This entry point has no counterpart in the model description; it is a service for
+ * callers that cannot allocate device memory: for example a host program that hands all
+ * device memory to its own pool at start-up and forbids any other allocation, a
+ * real-time loop that cannot afford the implicit device synchronisation cudaMalloc
+ * performs, or a small C host linked only against this library with no allocator of
+ * its own.  Instead of `ws`, the block's scratch lives in one statically sized device
+ * array inside the library (FLUX3_STATIC_SCRATCH_BYTES = 64 MiB); every GPU that loads
+ * the library holds that array until the process exits.
+ *  - Limit: the call needs flux3_block_workspace_size(dims, n_tokens) bytes of it; a
+ *    larger request returns FLUX3_ERR_WORKSPACE before anything runs.  At width 3072
+ *    (24 heads, SwiGLU 9216) that is about 48 KB per token, i.e. up to ~1,360 tokens.
+ *  - The first call on a device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the previous call's contents: calls
+ *    whose work overlaps on the GPU (other streams, other threads) race and corrupt each
+ *    other; serialise them.  Nothing in the array needs clearing: every scratch element
+ *    the kernels read is written earlier in the same call.
+ *  - Allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
+ * Other arguments and errors as flux3_block_fwd (one weight set, joint stage). */
+#define FLUX3_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+flux3_status flux3_block_fwd_static(const flux3_dims *dims, const flux3_block_weights *w,
+                                    const flux3_segments *segs, const void *x, void *x_out,
+                                    int32_t n_tokens, const float *rope, flux3_stream_t stream);
+
 /* Synchronises the device and reads the device error flags (bit 0: a bounded wait ran
  * out).  Returns FLUX3_ERR_TIMEOUT if any bit is set, else FLUX3_OK; flags may be NULL.
  * reset != 0 clears the flags.  Blocking; not for the hot path. */
