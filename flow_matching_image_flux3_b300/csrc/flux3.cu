@@ -284,22 +284,22 @@ flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const v
     P.n_tokens = N;
     P.heads = H;
     P.n_seg = n_seg;
-    int tiles = 0;
+    int pairs = 0;  // one CTA per pair of 128-query tiles of one segment and head
     for (int s = 0; s < n_seg; ++s) {
         P.seg_off[s] = off[s];
-        P.qt_begin[s] = tiles;
-        tiles += (off[s + 1] - off[s] + 127) / 128;
+        P.pair_begin[s] = pairs;
+        pairs += (off[s + 1] - off[s] + 255) / 256;
     }
     P.seg_off[n_seg] = off[n_seg];
-    P.qt_begin[n_seg] = tiles;
+    P.pair_begin[n_seg] = pairs;
     P.out = static_cast<__nv_bfloat16*>(out);
     P.ld_out = ld_out;
     P.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
-    if (tiles == 0) return FLUX3_OK;
+    if (pairs == 0) return FLUX3_OK;
     if (cudaFuncSetAttribute(attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_BYTES) != cudaSuccess)
         return FLUX3_ERR_CUDA;
     prof_before(FLUX3_KERNEL_ATTN, st);
-    attn_tcgen05_kernel<<<dim3(tiles, H), ATT_THREADS, ATT_SMEM_BYTES, st>>>(P);
+    attn_tcgen05_kernel<<<dim3(pairs, H), ATT_THREADS, ATT_SMEM_BYTES, st>>>(P);
     prof_after(st);
     return launch_status();
 }
