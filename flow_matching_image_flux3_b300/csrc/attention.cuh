@@ -39,6 +39,99 @@ struct AttnParams {
     float scale_log2;  // log2(e) / sqrt(128)
 };
 
+// ------------------------------------------------------------------ softmax arithmetic
+// Packed fp32 pairs (one 64-bit register, low word first) for the sm_100-family f32x2
+// instructions, which do two fp32 operations per issue slot.
+F3_DEV uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+F3_DEV void f2_split(uint64_t v, float& lo, float& hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
+F3_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+F3_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+F3_DEV uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+F3_DEV float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+F3_DEV uint32_t bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// 2^x for a pair on the FMA pipe instead of the MUFU unit (which alone would need as many
+// cycles as the tensor core for this kernel).  Range reduction x = j + f with j the
+// nearest integer (adding 1.5 * 2^23 leaves j in the low mantissa bits), f in [-1/2, 1/2];
+// 2^f from a cubic fitted for minimax relative error on [-1/2, 1/2] (max relative error
+// 7.5e-5, far below the bf16 rounding of P); 2^j is added to the exponent field.  x is
+// clamped at -125 so 2^j stays a normal number.
+F3_DEV void exp2_poly2(float x0, float x1, float& p0, float& p1) {
+    constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+    constexpr float c0 = 0.9999280571937561f, c1 = 0.6932608485221863f, c2 = 0.24261115491390228f,
+                    c3 = 0.05517221987247467f;
+    const uint64_t x = f2(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
+    const uint64_t t = f2_add(x, f2(kRound, kRound));
+    const uint64_t f = f2_sub(x, f2_sub(t, f2(kRound, kRound)));
+    uint64_t q = f2_fma(f2(c3, c3), f, f2(c2, c2));
+    q = f2_fma(q, f, f2(c1, c1));
+    q = f2_fma(q, f, f2(c0, c0));
+    float q0, q1, t0, t1;
+    f2_split(q, q0, q1);
+    f2_split(t, t0, t1);
+    p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+    p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+}
+
+#ifndef FLUX3_ATT_POLY_EVERY
+#define FLUX3_ATT_POLY_EVERY 0
+#endif
+
+// P = 2^(s * sc - m) for one 128-key row: every POLY-th pair goes through exp2_poly2 (0:
+// none), the rest through ex2.approx; P is stored as bf16 pairs over TMEM columns
+// 0..63 of the row's score tile.  Returns the row sum of P (fp32, before rounding).
+template <int POLY>
+F3_DEV float softmax_exp_store(const float (&s)[128], float sc, float m, uint32_t tS) {
+    const uint64_t sc2 = f2(sc, sc), nm2 = f2(-m, -m);
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int e = 64 * h + 2 * i;
+            float x0, x1, p0, p1;
+            f2_split(f2_fma(f2(s[e], s[e + 1]), sc2, nm2), x0, x1);
+            if (POLY > 0 && (i % POLY) == POLY - 1) {
+                exp2_poly2(x0, x1, p0, p1);
+            } else {
+                p0 = ex2(x0);
+                p1 = ex2(x1);
+            }
+            pk[i] = bf16x2(p0, p1);
+            acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
+        }
+        tmem_st32(tS + 32 * h, pk);
+    }
+    float a0, a1;
+    f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+    return a0 + a1;
+}
+
 __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -93,7 +186,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 8) {
+    if (warp >= 8) {
+        if (warp == 8) {
         if (lane == 0) {
             // ---------------- TMA producer
             const int nq = has_q1 ? 2 : 1;
@@ -134,7 +228,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                 }
             }
         }
-    } else if (warp == 9) {
+        } else if (warp == 9) {
         if (lane == 0) {
             // ---------------- MMA issuer
             constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
@@ -195,7 +289,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitTimeoutNs) {}
         }
-    } else if (warp < 4 || has_q1) {
+        }
+    } else {
+        if (warp < 4 || has_q1) {
         // ---------------- softmax of query tile t: one query row per thread
         const int t = warp >> 2;
         const int sub = warp & 3;
@@ -225,17 +321,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                 }
             }
             const int k0 = kv0 + 128 * j;
-            if (!(k0 >= seg_lo && k0 + 128 <= seg_hi)) {
+            const bool full = k0 >= seg_lo && k0 + 128 <= seg_hi;
+            if (!full) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i) {
                     const int key = k0 + i;
                     if (key < seg_lo || key >= seg_hi) s[i] = -INFINITY;
                 }
             }
-            float mx = s[0];
+            // row max: four independent chains of 3-input max
+            float ma = s[0], mb = s[1], mc = s[2], md = s[3];
 #pragma unroll
-            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
-            mx *= sc;
+            for (int i = 4; i < 124; i += 8) {
+                ma = max3(ma, s[i], s[i + 1]);
+                mb = max3(mb, s[i + 2], s[i + 3]);
+                mc = max3(mc, s[i + 4], s[i + 5]);
+                md = max3(md, s[i + 6], s[i + 7]);
+            }
+            ma = max3(ma, s[124], s[125]);
+            mb = max3(mb, s[126], s[127]);
+            const float mx = max3(ma, mb, fmaxf(mc, md)) * sc;
             // keep the stale max unless the new one exceeds it by the slack
             const float mnew = (mx > m + ATT_RESCALE_LOG2) ? mx : m;
             if (j > 0 && __any_sync(0xffffffffu, mnew != m)) {
@@ -253,20 +358,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                 l *= alpha;
             }
             m = mnew;
-            const float nm = -m;
-            float sum = 0.f;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2(fmaf(s[64 * h + 2 * i], sc, nm));
-                    const float p1 = ex2(fmaf(s[64 * h + 2 * i + 1], sc, nm));
-                    sum += p0 + p1;
-                    pk[i] = pack_bf16(p0, p1);
-                }
-                tmem_st32(tS + 32 * h, pk);
-            }
+            // masked tiles hold -inf scores: they take the exact ex2 path throughout
+            const float sum = full ? softmax_exp_store<FLUX3_ATT_POLY_EVERY>(s, sc, m, tS)
+                                   : softmax_exp_store<0>(s, sc, m, tS);
             l += sum;
             tmem_st_wait();
             tc_fence_before();
@@ -295,6 +389,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                 }
             }
         }
+    }
     }
     tc_fence_before();
     __syncthreads();
