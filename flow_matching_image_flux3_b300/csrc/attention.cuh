@@ -186,24 +186,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp >= 8) {
-        if (warp == 8) {
-        if (lane == 0) {
-            // ---------------- TMA producer
-            const int nq = has_q1 ? 2 : 1;
+    if (warp == 8) {
+        // ---------------- TMA producer (converged warp, one elected lane issues)
+        const bool leader = elect_one();
+        const int nq = has_q1 ? 2 : 1;
+        if (leader) {
             for (int t = 0; t < nq; ++t) {
                 mbar_arrive_expect_tx(q_full(t), ATT_TILE_BYTES);
                 tma_load_3d(sQ(t), &p.tm_q, q_full(t), 0, q0 + 128 * t, head);
                 tma_load_3d(sQ(t) + 16384, &p.tm_q, q_full(t), 64, q0 + 128 * t, head);
             }
-            int issued = 0;
-            bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int k0 = kv0 + 128 * j;
-                for (int which = 0; which < 2; ++which) {
-                    const int idx = 2 * j + which;
-                    const int slot = idx % ATT_SLOTS;
-                    if (!mbar_wait(kv_empty(slot), ((idx / ATT_SLOTS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        }
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < nkv && ok; ++j) {
+            const int k0 = kv0 + 128 * j;
+            for (int which = 0; which < 2; ++which) {
+                const int idx = 2 * j + which;
+                const int slot = idx % ATT_SLOTS;
+                if (!mbar_wait_warp(kv_empty(slot), ((idx / ATT_SLOTS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (leader) {
                     mbar_arrive_expect_tx(kv_full(slot), ATT_TILE_BYTES);
                     if (which == 0) {
                         tma_load_3d(sKV(slot), &p.tm_k, kv_full(slot), 0, k0, head);
@@ -212,29 +214,31 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                         tma_load_3d(sKV(slot), &p.tm_v, kv_full(slot), k0, 0, head);
                         tma_load_3d(sKV(slot) + 16384, &p.tm_v, kv_full(slot), k0 + 64, 0, head);
                     }
-                    ++issued;
                 }
-            }
-            if (!ok) {
-                // let the copies in flight land before the CTA exits
-                for (int t = 0; t < nq; ++t) {
-                    const unsigned long long t0 = globaltimer();
-                    while (!mbar_try_wait(q_full(t), 0) && globaltimer() - t0 < kWaitTimeoutNs) {}
-                }
-                for (int idx = issued - 1; idx >= 0 && idx >= issued - ATT_SLOTS; --idx) {
-                    const unsigned long long t1 = globaltimer();
-                    while (!mbar_try_wait(kv_full(idx % ATT_SLOTS), (idx / ATT_SLOTS) & 1) &&
-                           globaltimer() - t1 < kWaitTimeoutNs) {}
-                }
+                __syncwarp();
+                ++issued;
             }
         }
-        } else if (warp == 9) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
-            const int nq = has_q1 ? 2 : 1;
-            // S_t = Q_t K^T for the K tile in `slot`
-            auto qk = [&](int t, int slot) {
+        if (!ok && leader) {
+            // let the copies in flight land before the CTA exits
+            for (int t = 0; t < nq; ++t) {
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(q_full(t), 0) && globaltimer() - t0 < kWaitTimeoutNs) {}
+            }
+            for (int idx = issued - 1; idx >= 0 && idx >= issued - ATT_SLOTS; --idx) {
+                const unsigned long long t1 = globaltimer();
+                while (!mbar_try_wait(kv_full(idx % ATT_SLOTS), (idx / ATT_SLOTS) & 1) &&
+                       globaltimer() - t1 < kWaitTimeoutNs) {}
+            }
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issuer (converged warp, one elected lane issues)
+        const bool leader = elect_one();
+        constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+        const int nq = has_q1 ? 2 : 1;
+        // S_t = Q_t K^T for the K tile in `slot`
+        auto qk = [&](int t, int slot) {
+            if (leader) {
                 const uint64_t qd = sdesc_kmajor_sw128(sQ(t)), kd = sdesc_kmajor_sw128(sKV(slot));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -242,54 +246,64 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                     mma_bf16_ss(tmem + t * 128, qd + off, kd + off, IDESC, kk > 0);
                 }
                 mma_commit(s_full(t));
-            };
-            // O_t += P_t V for the V^T tile in `slot`; P_t is bf16 in columns 0..63 of S_t
-            auto pv = [&](int t, int slot, bool acc) {
+            }
+            __syncwarp();
+        };
+        // O_t += P_t V for the V^T tile in `slot`; P_t is bf16 in columns 0..63 of S_t
+        auto pv = [&](int t, int slot, bool acc) {
+            if (leader) {
                 const uint64_t vd = sdesc_kmajor_sw128(sKV(slot));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
                     mma_bf16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd + off, IDESC, acc || kk > 0);
                 }
-            };
-            bool ok = mbar_wait(q_full(0), 0, abort_flag) && mbar_wait(kv_full(0), 0, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                qk(0, 0);
-                if (has_q1) {
-                    ok = mbar_wait(q_full(1), 0, abort_flag);
-                    if (ok) {
-                        tc_fence_after();
-                        qk(1, 0);
-                    }
-                }
-                mma_commit(kv_empty(0));
             }
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int vidx = 2 * j + 1, vslot = vidx % ATT_SLOTS;
-                const int kidx = 2 * j + 2, kslot = kidx % ATT_SLOTS;
-                const bool more = j + 1 < nkv;
-                if (!mbar_wait(kv_full(vslot), (vidx / ATT_SLOTS) & 1, abort_flag)) { ok = false; break; }
-                if (more && !mbar_wait(kv_full(kslot), (kidx / ATT_SLOTS) & 1, abort_flag)) { ok = false; break; }
-                for (int t = 0; t < nq; ++t) {
-                    if (!mbar_wait(p_full(t), j & 1, abort_flag)) { ok = false; break; }
+            __syncwarp();
+        };
+        auto commit = [&](uint32_t bar) {
+            if (leader) mma_commit(bar);
+            __syncwarp();
+        };
+        bool ok = mbar_wait_warp(q_full(0), 0, abort_flag) && mbar_wait_warp(kv_full(0), 0, abort_flag);
+        if (ok) {
+            tc_fence_after();
+            qk(0, 0);
+            if (has_q1) {
+                ok = mbar_wait_warp(q_full(1), 0, abort_flag);
+                if (ok) {
                     tc_fence_after();
-                    pv(t, vslot, j > 0);
-                    if (more) qk(t, kslot);  // runs after the P V that reads S_t's columns
+                    qk(1, 0);
                 }
-                if (!ok) break;
-                mma_commit(kv_empty(vslot));
-                if (more) mma_commit(kv_empty(kslot));
             }
-            if (ok) {
-                mma_commit(o_full(0));
-                if (has_q1) mma_commit(o_full(1));
+            commit(kv_empty(0));
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+            const int vidx = 2 * j + 1, vslot = vidx % ATT_SLOTS;
+            const int kidx = 2 * j + 2, kslot = kidx % ATT_SLOTS;
+            const bool more = j + 1 < nkv;
+            if (!mbar_wait_warp(kv_full(vslot), (vidx / ATT_SLOTS) & 1, abort_flag)) { ok = false; break; }
+            if (more && !mbar_wait_warp(kv_full(kslot), (kidx / ATT_SLOTS) & 1, abort_flag)) { ok = false; break; }
+            for (int t = 0; t < nq; ++t) {
+                if (!mbar_wait_warp(p_full(t), j & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                pv(t, vslot, j > 0);
+                if (more) qk(t, kslot);  // runs after the P V that reads S_t's columns
             }
-            mma_commit(drain);
+            if (!ok) break;
+            commit(kv_empty(vslot));
+            if (more) commit(kv_empty(kslot));
+        }
+        if (ok) {
+            commit(o_full(0));
+            if (has_q1) commit(o_full(1));
+        }
+        commit(drain);
+        if (leader) {
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitTimeoutNs) {}
         }
-        }
+        __syncwarp();
     } else {
         if (warp < 4 || has_q1) {
         // ---------------- softmax of query tile t: one query row per thread

@@ -7,9 +7,9 @@
 //   EPI_F32             plain fp32 store (+ bias): the output layer
 //
 // Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads, warp 1 issues
-// tcgen05.mma from one thread and owns the TMEM allocation, warps 2..5 run the
-// epilogue, one accumulator row (TMEM lane) per thread.  Two TMEM accumulators let
-// the epilogue of one tile overlap the MMAs of the next.
+// tcgen05.mma and owns the TMEM allocation (both run as converged warps with one elected
+// lane issuing), warps 2..5 run the epilogue, one accumulator row (TMEM lane) per thread.
+// Two TMEM accumulators let the epilogue of one tile overlap the MMAs of the next.
 #pragma once
 #include <cuda.h>
 #include "sm103.cuh"
@@ -300,59 +300,62 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
     const int total = p.m_tiles * p.n_tiles;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer
-            int s = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const int n = t / p.m_tiles, mt = t - (t / p.m_tiles) * p.m_tiles;
-                const int g = group_of_tile(p, mt);
-                const int row0 = p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM;
-                const CUtensorMap* tb = &p.tm_b[p.grp[g].wset];
-                int r0, r1;
-                b_rows<BN, EPI>(p, n, r0, r1);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+        // ---------------- TMA producer (converged warp, one elected lane issues)
+        const bool leader = elect_one();
+        int s = 0;
+        uint32_t ph = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const int n = t / p.m_tiles, mt = t - (t / p.m_tiles) * p.m_tiles;
+            const int g = group_of_tile(p, mt);
+            const int row0 = p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM;
+            const CUtensorMap* tb = &p.tm_b[p.grp[g].wset];
+            int r0, r1;
+            b_rows<BN, EPI>(p, n, r0, r1);
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+                if (leader) {
                     const uint32_t sa = smem_base + s * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
                     mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
                     tma_load_2d(sa, &p.tm_a, full_bar(s), kb * GEMM_BK, row0);
                     tma_load_2d(sb, tb, full_bar(s), kb * GEMM_BK, r0);
                     if (BN == 256) tma_load_2d(sb + 128 * 128, tb, full_bar(s), kb * GEMM_BK, r1);
-                    ++issued;
-                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                 }
+                __syncwarp();
+                ++issued;
+                if (++s == C::STAGES) { s = 0; ph ^= 1u; }
             }
-            if (!ok) {
-                // let the copies already in flight land before the CTA exits
-                int back = issued < C::STAGES ? issued : C::STAGES;
-                int ss = s;
-                uint32_t pp = ph;
-                for (int i = 0; i < back; ++i) {
-                    if (--ss < 0) { ss = C::STAGES - 1; pp ^= 1u; }
-                    const unsigned long long t0 = globaltimer();
-                    while (!mbar_try_wait(full_bar(ss), pp) && globaltimer() - t0 < kWaitTimeoutNs) {}
-                }
+        }
+        if (!ok && leader) {
+            // let the copies already in flight land before the CTA exits
+            int back = issued < C::STAGES ? issued : C::STAGES;
+            int ss = s;
+            uint32_t pp = ph;
+            for (int i = 0; i < back; ++i) {
+                if (--ss < 0) { ss = C::STAGES - 1; pp ^= 1u; }
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(full_bar(ss), pp) && globaltimer() - t0 < kWaitTimeoutNs) {}
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN);
-            int s = 0;
-            uint32_t ph = 0;
-            int acc = 0;
-            uint32_t aph = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) { ok = false; break; }
+        // ---------------- MMA issuer (converged warp, one elected lane issues)
+        const bool leader = elect_one();
+        constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN);
+        int s = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            if (!mbar_wait_warp(tempty_bar(acc), aph ^ 1u, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem_base + acc * BN;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_warp(full_bar(s), ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(full_bar(s), ph, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+                if (leader) {
                     const uint32_t sa = smem_base + s * C::STAGE_BYTES;
                     const uint64_t ad = sdesc_kmajor_sw128(sa);
                     const uint64_t bd = sdesc_kmajor_sw128(sa + C::A_BYTES);
@@ -360,17 +363,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
                     for (int k = 0; k < GEMM_BK / 16; ++k)
                         mma_bf16_ss(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
                     mma_commit(empty_bar(s));
-                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                 }
-                if (!ok) break;
-                mma_commit(tfull_bar(acc));
-                if (++acc == 2) { acc = 0; aph ^= 1u; }
+                __syncwarp();
+                if (++s == C::STAGES) { s = 0; ph ^= 1u; }
             }
-            // all issued MMAs retire before TMEM is released
+            if (!ok) break;
+            if (leader) mma_commit(tfull_bar(acc));
+            __syncwarp();
+            if (++acc == 2) { acc = 0; aph ^= 1u; }
+        }
+        // all issued MMAs retire before TMEM is released
+        if (leader) {
             mma_commit(drain_bar);
             const unsigned long long t0 = globaltimer();
             while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < kWaitTimeoutNs) {}
         }
+        __syncwarp();
     } else {
         // ---------------- epilogue warps 2..5
         const int sub = warp & 3;  // TMEM lane quarter this warp may access

@@ -83,6 +83,13 @@ F3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     }
 }
 
+// The same wait executed by a whole converged warp; the result is uniform across the warp.
+// (A role loop run by one lane while the other 31 sit elsewhere pays about 100 cycles per
+// mbarrier check; a converged warp with one elected lane issuing pays a few.)
+F3_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+}
+
 // ------------------------------------------------------------------ TMA
 F3_DEV void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
