@@ -180,34 +180,83 @@ flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& 
     return launch_status();
 }
 
+// Clusters of two CTAs that can be resident at once for a GEMM instantiation (SMs are
+// paired within a GPC, so this can be below half the SM count); cached per device.
 template <int BN, int EPI>
+int max_active_pairs(int smem, int sms) {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] > 0) return cache[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms & ~1));
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<BN, EPI, 2>, &cfg) != cudaSuccess) return 0;
+    cache[dev] = n;
+    return n;
+}
+
+template <int BN, int EPI, int CL>
 flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
-    const int total = P.m_tiles * P.n_tiles;
-    if (total == 0) return FLUX3_OK;
+    const int tasks = (P.m_tiles / CL) * P.n_tiles;
+    if (tasks == 0) return FLUX3_OK;
     const int smem = GemmCfg<BN>::SMEM_BYTES;
-    if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, EPI, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return FLUX3_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return FLUX3_ERR_CUDA;
-    const int grid = total < sms ? total : sms;
+    if constexpr (CL == 1) {
+        const int grid = tasks < sms ? tasks : sms;
+        prof_before(kind, st);
+        gemm_tcgen05_kernel<BN, EPI, CL><<<grid, GEMM_THREADS, smem, st>>>(P);
+        prof_after(st);
+        return launch_status();
+    } else {
+    const int pairs = max_active_pairs<BN, EPI>(smem, sms);
+    if (pairs <= 0) return FLUX3_ERR_CUDA;
+    const int units = tasks < pairs ? tasks : pairs;  // persistent: every cluster resident at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * units));
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     prof_before(kind, st);
-    gemm_tcgen05_kernel<BN, EPI><<<grid, GEMM_THREADS, smem, st>>>(P);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, EPI, CL>, P);
     prof_after(st);
-    return launch_status();
+    return e == cudaSuccess ? launch_status() : FLUX3_ERR_CUDA;
+    }
 }
 
-// groups of rows sharing one weight set; m-tiles never straddle a group
-void fill_groups(GemmParams& P, const int32_t* off, int n_seg, int n_w, int N) {
+// groups of rows sharing one weight set; m-tiles never straddle a group, and with clusters
+// of `cl` CTAs every group starts on a multiple of cl (a cluster's tiles share weights)
+void fill_groups(GemmParams& P, const int32_t* off, int n_seg, int n_w, int N, int cl) {
+    auto units = [cl](int rows) { return ((rows + GEMM_BM - 1) / GEMM_BM + cl - 1) / cl * cl; };
     int tiles = 0;
     if (n_w == 1) {
         P.n_groups = 1;
         P.grp[0] = {0, N, 0, 0};
-        tiles = (N + GEMM_BM - 1) / GEMM_BM;
+        tiles = units(N);
     } else {
         P.n_groups = n_seg;
         for (int s = 0; s < n_seg; ++s) {
             P.grp[s] = {off[s], off[s + 1], tiles, s};
-            tiles += (off[s + 1] - off[s] + GEMM_BM - 1) / GEMM_BM;
+            tiles += units(off[s + 1] - off[s]);
         }
     }
     P.m_tiles = tiles;
@@ -225,7 +274,7 @@ flux3_status run_in_proj(const flux3_dims* d, const flux3_block_weights* w, int 
         if (!tmap_2d(&P.tm_b[i], w[i].w_in, D, n_in, (uint64_t)D * 2, 128)) return FLUX3_ERR_INVALID_ARG;
         P.ew[i] = {w[i].b_in, w[i].q_norm, w[i].k_norm};
     }
-    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N);
+    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N, 2);
     P.n_tiles = 3 * H / 2 + F / 128;
     P.k_blocks = D / GEMM_BK;
     P.heads = H; P.width = D; P.ffn = F; P.n_tokens = N; P.ld_vt = ld_vt; P.ld_y = D + F;
@@ -233,7 +282,7 @@ flux3_status run_in_proj(const flux3_dims* d, const flux3_block_weights* w, int 
     P.rope = rope;
     P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
     P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
-    return launch_gemm<256, EPI_QKV_SWIGLU>(P, st, FLUX3_KERNEL_IN_PROJ);
+    return launch_gemm<256, EPI_QKV_SWIGLU, 2>(P, st, FLUX3_KERNEL_IN_PROJ);
 }
 
 flux3_status run_out_proj(const flux3_dims* d, const flux3_block_weights* w, int n_w, const flux3_segments* segs, const void* y,
@@ -248,7 +297,7 @@ flux3_status run_out_proj(const flux3_dims* d, const flux3_block_weights* w, int
         if (!tmap_2d(&P.tm_b[i], w[i].w_out, K, D, (uint64_t)K * 2, 128)) return FLUX3_ERR_INVALID_ARG;
         P.ew[i] = {w[i].b_out, nullptr, nullptr};
     }
-    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N);
+    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N, 2);
     P.n_tiles = D / 256;
     P.k_blocks = K / GEMM_BK;
     P.width = D;
@@ -257,7 +306,7 @@ flux3_status run_out_proj(const flux3_dims* d, const flux3_block_weights* w, int
     P.mod = segs->mod;
     P.n_seg = segs->n_seg;
     for (int i = 0; i <= segs->n_seg; ++i) P.seg_off[i] = segs->seg_off[i];
-    return launch_gemm<256, EPI_GATED_RESIDUAL>(P, st, FLUX3_KERNEL_OUT_PROJ);
+    return launch_gemm<256, EPI_GATED_RESIDUAL, 2>(P, st, FLUX3_KERNEL_OUT_PROJ);
 }
 
 flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const void* vt, int ld_vt, int N, const int32_t* off,
@@ -351,7 +400,7 @@ flux3_status run_final(const flux3_dims* d, const void* w_final, const float* b_
     P.width = D;
     P.out = out;
     P.ld_out = out_ch;
-    return launch_gemm<128, EPI_F32>(P, st, FLUX3_KERNEL_FINAL);
+    return launch_gemm<128, EPI_F32, 1>(P, st, FLUX3_KERNEL_FINAL);
 }
 
 }  // namespace
@@ -408,7 +457,11 @@ flux3_status flux3_rope_build(const flux3_dims* dims, const int32_t* pos, int32_
     const long long total = (long long)n_tokens * 64;
     prof_before(FLUX3_KERNEL_ROPE, st);
     RopeFreqs fr;
-    for (int j = 0; j < 16; ++j) fr.f[j] = std::pow((double)dims->rope_theta, -(double)(2 * j) / 32.0);
+    for (int j = 0; j < 16; ++j) {
+        const double g = std::pow((double)dims->rope_theta, -(double)(2 * j) / 32.0) / 6.283185307179586476925286766559;
+        fr.hi[j] = (float)g;
+        fr.lo[j] = (float)(g - (double)fr.hi[j]);
+    }
     rope_table_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(pos, n_tokens, fr, reinterpret_cast<float2*>(rope));
     prof_after(st);
     return launch_status();

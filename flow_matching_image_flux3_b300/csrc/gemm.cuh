@@ -255,8 +255,27 @@ F3_DEV void epi_f32(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
 }
 
 // --------------------------------------------------------------------- the kernel
-template <int BN, int EPI>
+// Tiles are numbered n-major (all m-tiles of one weight tile run together, so each weight
+// tile is read from HBM once).  With CL = 2 the kernel runs as clusters of two CTAs that
+// take adjacent m-tiles of the same weight tile: each CTA loads its own A tile and one
+// 128-row half of the shared B tile, multicast into both CTAs' shared memory, which cuts
+// each SM's L2 reads per k-block from 48 KB to 32 KB.  A stage is free only when both CTAs'
+// MMAs have read it: every MMA commit arrives on the slot barrier of both CTAs.  Groups of
+// the grouped GEMM then start on an even m-tile, so a pair never straddles two weight sets.
+struct TileInfo {
+    int n, g, row0;
+};
+F3_DEV TileInfo tile_info(const GemmParams& p, int task, int rank, int cl) {
+    const int m_units = p.m_tiles / cl;
+    const int n = task / m_units;
+    const int mt = (task - n * m_units) * cl + rank;
+    const int g = group_of_tile(p, mt);
+    return {n, g, p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM};
+}
+
+template <int BN, int EPI, int CL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+    static_assert(CL == 1 || (CL == 2 && BN == 256), "clusters of two split a 256-row B tile");
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -273,10 +292,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
+    const int unit = blockIdx.x / CL, n_units = gridDim.x / CL;  // cluster index and count
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CL);  // one MMA commit from each CTA of the cluster
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -294,10 +315,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (CL > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const int total = p.m_tiles * p.n_tiles;
+    const int tasks = (p.m_tiles / CL) * p.n_tiles;
+    constexpr uint16_t kPair = 0x3;
 
     if (warp == 0) {
         // ---------------- TMA producer (converged warp, one elected lane issues)
@@ -306,22 +329,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         uint32_t ph = 0;
         int issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const int n = t / p.m_tiles, mt = t - (t / p.m_tiles) * p.m_tiles;
-            const int g = group_of_tile(p, mt);
-            const int row0 = p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM;
-            const CUtensorMap* tb = &p.tm_b[p.grp[g].wset];
+        for (int task = unit; task < tasks && ok; task += n_units) {
+            const TileInfo ti = tile_info(p, task, rank, CL);
+            const CUtensorMap* tb = &p.tm_b[p.grp[ti.g].wset];
             int r0, r1;
-            b_rows<BN, EPI>(p, n, r0, r1);
+            b_rows<BN, EPI>(p, ti.n, r0, r1);
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 if (!mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
                 if (leader) {
                     const uint32_t sa = smem_base + s * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
                     mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-                    tma_load_2d(sa, &p.tm_a, full_bar(s), kb * GEMM_BK, row0);
-                    tma_load_2d(sb, tb, full_bar(s), kb * GEMM_BK, r0);
-                    if (BN == 256) tma_load_2d(sb + 128 * 128, tb, full_bar(s), kb * GEMM_BK, r1);
+                    tma_load_2d(sa, &p.tm_a, full_bar(s), kb * GEMM_BK, ti.row0);
+                    if (CL == 2) {
+                        tma_load_2d_multicast(sb + rank * 128 * 128, tb, full_bar(s), kb * GEMM_BK, rank ? r1 : r0, kPair);
+                    } else {
+                        tma_load_2d(sb, tb, full_bar(s), kb * GEMM_BK, r0);
+                        if (BN == 256) tma_load_2d(sb + 128 * 128, tb, full_bar(s), kb * GEMM_BK, r1);
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -348,7 +373,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         int acc = 0;
         uint32_t aph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int task = unit; task < tasks && ok; task += n_units) {
             if (!mbar_wait_warp(tempty_bar(acc), aph ^ 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + acc * BN;
@@ -362,7 +387,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
 #pragma unroll
                     for (int k = 0; k < GEMM_BK / 16; ++k)
                         mma_bf16_ss(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
-                    mma_commit(empty_bar(s));
+                    if (CL == 2) mma_commit_multicast(empty_bar(s), kPair);
+                    else mma_commit(empty_bar(s));
                 }
                 __syncwarp();
                 if (++s == C::STAGES) { s = 0; ph ^= 1u; }
@@ -384,19 +410,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         const int sub = warp & 3;  // TMEM lane quarter this warp may access
         int acc = 0;
         uint32_t aph = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const int n = t / p.m_tiles, mt = t - (t / p.m_tiles) * p.m_tiles;
-            const int g = group_of_tile(p, mt);
-            const int row0 = p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM;
-            const int r = row0 + sub * 32 + lane;
-            const bool valid = r < p.grp[g].row_end;
+        for (int task = unit; task < tasks; task += n_units) {
+            const TileInfo ti = tile_info(p, task, rank, CL);
+            const int r = ti.row0 + sub * 32 + lane;
+            const bool valid = r < p.grp[ti.g].row_end;
             if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16) + acc * BN;
-            const EpiWeights& w = p.ew[p.grp[g].wset];
-            if (EPI == EPI_QKV_SWIGLU) epi_qkv(p, w, n, tacc, valid ? r : 0, valid);
-            else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, n, tacc, valid ? r : 0, valid);
-            else epi_f32<BN>(p, w, n, tacc, valid ? r : 0, valid);
+            const EpiWeights& w = p.ew[p.grp[ti.g].wset];
+            if (EPI == EPI_QKV_SWIGLU) epi_qkv(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -409,6 +433,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    if (CL > 1) cluster_sync();  // no CTA leaves while its peer may still signal it
 }
 
 }  // namespace f3

@@ -107,6 +107,27 @@ F3_DEV void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0, in
         : "memory");
 }
 
+// The same 2D load delivered to the same shared-memory offset in every CTA of the cluster
+// named by cta_mask, each destination's mbarrier (same offset) receiving the bytes.
+F3_DEV void tma_load_2d_multicast(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+        : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+F3_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster arrive and wait (release / acquire).
+F3_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // generic-proxy shared-memory writes -> visible to the async proxy (tensor core reads)
 F3_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -143,6 +164,14 @@ F3_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32
 // Arrive once on the mbarrier when all previously issued tcgen05 ops of this thread finish.
 F3_DEV void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive once on the mbarrier at this offset in every CTA of cta_mask when all previously
+// issued tcgen05 ops of this thread finish.
+F3_DEV void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+                 "h"(cta_mask)
+                 : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32*(w%4)..).
