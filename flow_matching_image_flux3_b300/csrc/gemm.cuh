@@ -262,15 +262,19 @@ F3_DEV void epi_f32(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
 // each SM's L2 reads per k-block from 48 KB to 32 KB.  A stage is free only when both CTAs'
 // MMAs have read it: every MMA commit arrives on the slot barrier of both CTAs.  Groups of
 // the grouped GEMM then start on an even m-tile, so a pair never straddles two weight sets.
+// The clusters that share a weight tile run in near lockstep; each walks the K dimension
+// from its own starting k-block (spread evenly by m index), so a weight k-block's first
+// read from DRAM stalls one cluster rather than all of them at once.
 struct TileInfo {
-    int n, g, row0;
+    int n, g, row0, kb0;
 };
 F3_DEV TileInfo tile_info(const GemmParams& p, int task, int rank, int cl) {
     const int m_units = p.m_tiles / cl;
     const int n = task / m_units;
-    const int mt = (task - n * m_units) * cl + rank;
+    const int mu = task - n * m_units;
+    const int mt = mu * cl + rank;
     const int g = group_of_tile(p, mt);
-    return {n, g, p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM};
+    return {n, g, p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM, (int)((long long)mu * p.k_blocks / m_units)};
 }
 
 template <int BN, int EPI, int CL>
@@ -339,13 +343,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
                 if (leader) {
                     const uint32_t sa = smem_base + s * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
+                    int kr = ti.kb0 + kb;
+                    if (kr >= p.k_blocks) kr -= p.k_blocks;
+                    const int kc = kr * GEMM_BK;
                     mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-                    tma_load_2d(sa, &p.tm_a, full_bar(s), kb * GEMM_BK, ti.row0);
+                    tma_load_2d(sa, &p.tm_a, full_bar(s), kc, ti.row0);
                     if (CL == 2) {
-                        tma_load_2d_multicast(sb + rank * 128 * 128, tb, full_bar(s), kb * GEMM_BK, rank ? r1 : r0, kPair);
+                        tma_load_2d_multicast(sb + rank * 128 * 128, tb, full_bar(s), kc, rank ? r1 : r0, kPair);
                     } else {
-                        tma_load_2d(sb, tb, full_bar(s), kb * GEMM_BK, r0);
-                        if (BN == 256) tma_load_2d(sb + 128 * 128, tb, full_bar(s), kb * GEMM_BK, r1);
+                        tma_load_2d(sb, tb, full_bar(s), kc, r0);
+                        if (BN == 256) tma_load_2d(sb + 128 * 128, tb, full_bar(s), kc, r1);
                     }
                 }
                 __syncwarp();
