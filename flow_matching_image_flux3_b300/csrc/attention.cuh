@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
         float m = -INFINITY, l = 0.f;  // running max (log2 units, scaled) and sum
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            if (!mbar_wait(s_full(t), j & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(s_full(t), j & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             float s[128];
             {
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(t));
         }
-        if (ok && mbar_wait(o_full(t), 0, abort_flag)) {
+        if (ok && mbar_wait_warp(o_full(t), 0, abort_flag)) {
             tc_fence_after();
             const int qrow = q0 + 128 * t + row;
             const bool valid = qrow < seg_hi;

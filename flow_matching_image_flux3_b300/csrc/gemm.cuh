@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
             const TileInfo ti = tile_info(p, task, rank, CL);
             const int r = ti.row0 + sub * 32 + lane;
             const bool valid = r < p.grp[ti.g].row_end;
-            if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
+            if (!mbar_wait_warp(tfull_bar(acc), aph, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16) + acc * BN;
             const EpiWeights& w = p.ew[p.grp[ti.g].wset];

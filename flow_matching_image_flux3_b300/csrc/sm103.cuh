@@ -83,10 +83,26 @@ F3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     }
 }
 
+// Non-blocking: has the phase with this parity completed?
+F3_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // The same wait executed by a whole converged warp; the result is uniform across the warp.
-// (A role loop run by one lane while the other 31 sit elsewhere pays about 100 cycles per
-// mbarrier check; a converged warp with one elected lane issuing pays a few.)
+// The common case (phase already complete) is one test and a vote, about 30 cycles; going
+// straight into the bounded wait loop costs about 90 even then.  (A role loop run by one
+// lane while the other 31 sit elsewhere pays about 100 cycles per check; a converged warp
+// with one elected lane issuing pays a few.)
 F3_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
 }
 
