@@ -101,15 +101,15 @@ F3_DEV void exp2_poly2(float x0, float x1, float& p0, float& p1) {
 #define FLUX3_ATT_POLY_EVERY 0
 #endif
 
-// P = 2^(s * sc - m) for one 128-key row: every POLY-th pair goes through exp2_poly2 (0:
-// none), the rest through ex2.approx; P is stored as bf16 pairs over TMEM columns
-// 0..63 of the row's score tile.  Returns the row sum of P (fp32, before rounding).
+// P = 2^(s * sc - m) for keys 64 h .. 64 h + 63 of one 128-key row: every POLY-th pair
+// goes through exp2_poly2 (0: none), the rest through ex2.approx; P is stored as bf16
+// pairs over TMEM columns 32 h .. 32 h + 31 of the row's score tile.  Returns the sum of
+// those 64 P values (fp32, before rounding).
 template <int POLY>
-F3_DEV float softmax_exp_store(const float (&s)[128], float sc, float m, uint32_t tS) {
+F3_DEV float softmax_exp_store(const float (&s)[128], int h, float sc, float m, uint32_t tS) {
     const uint64_t sc2 = f2(sc, sc), nm2 = f2(-m, -m);
     uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
     auto p_full = [&](int t) { return b0 + 8u * (4 + 2 * ATT_SLOTS + t); };
     auto o_full = [&](int t) { return b0 + 8u * (6 + 2 * ATT_SLOTS + t); };
     const uint32_t drain = b0 + 8u * (8 + 2 * ATT_SLOTS);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9 + 2 * ATT_SLOTS);
+    auto p_half = [&](int t) { return b0 + 8u * (9 + 2 * ATT_SLOTS + t); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11 + 2 * ATT_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
             mbar_init(q_full(t), 1);
             mbar_init(s_full(t), 1);
             mbar_init(p_full(t), 4);
+            mbar_init(p_half(t), 4);
             mbar_init(o_full(t), 1);
         }
         for (int s = 0; s < ATT_SLOTS; ++s) {
@@ -238,33 +240,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
         const int nq = has_q1 ? 2 : 1;
         // S_t = Q_t K^T for the K tile in `slot`
         auto qk = [&](int t, int slot) {
-            if (leader) {
-                const uint64_t qd = sdesc_kmajor_sw128(sQ(t)), kd = sdesc_kmajor_sw128(sKV(slot));
+            const uint64_t qd = sdesc_kmajor_sw128(sQ(t)), kd = sdesc_kmajor_sw128(sKV(slot));
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_bf16_ss(tmem + t * 128, qd + off, kd + off, IDESC, kk > 0);
-                }
-                mma_commit(s_full(t));
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_bf16_ss_if(leader, tmem + t * 128, qd + off, kd + off, IDESC, kk > 0);
             }
-            __syncwarp();
+            mma_commit_if(leader, s_full(t));
         };
         // O_t += P_t V for the V^T tile in `slot`; P_t is bf16 in columns 0..63 of S_t
-        auto pv = [&](int t, int slot, bool acc) {
-            if (leader) {
-                const uint64_t vd = sdesc_kmajor_sw128(sKV(slot));
+        // (keys 64 h .. 64 h + 63: the half in V^T's swizzle atom h, P columns 32 h ..)
+        auto pv = [&](int t, int slot, int h, bool acc) {
+            const uint64_t vd = sdesc_kmajor_sw128(sKV(slot));
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_bf16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd + off, IDESC, acc || kk > 0);
-                }
+            for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_bf16_ts_if(leader, tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd + off, IDESC, acc || kk > 0);
             }
-            __syncwarp();
         };
-        auto commit = [&](uint32_t bar) {
-            if (leader) mma_commit(bar);
-            __syncwarp();
-        };
+        auto commit = [&](uint32_t bar) { mma_commit_if(leader, bar); };
         bool ok = mbar_wait_warp(q_full(0), 0, abort_flag) && mbar_wait_warp(kv_full(0), 0, abort_flag);
         if (ok) {
             tc_fence_after();
@@ -285,9 +279,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
             if (!mbar_wait_warp(kv_full(vslot), (vidx / ATT_SLOTS) & 1, abort_flag)) { ok = false; break; }
             if (more && !mbar_wait_warp(kv_full(kslot), (kidx / ATT_SLOTS) & 1, abort_flag)) { ok = false; break; }
             for (int t = 0; t < nq; ++t) {
+                // the first half of P V starts while the softmax still computes the second
+                if (!mbar_wait_warp(p_half(t), j & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                pv(t, vslot, 0, j > 0);
                 if (!mbar_wait_warp(p_full(t), j & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                pv(t, vslot, j > 0);
+                pv(t, vslot, 1, true);
                 if (more) qk(t, kslot);  // runs after the P V that reads S_t's columns
             }
             if (!ok) break;
@@ -343,18 +341,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                     if (key < seg_lo || key >= seg_hi) s[i] = -INFINITY;
                 }
             }
-            // row max: four independent chains of 3-input max
-            float ma = s[0], mb = s[1], mc = s[2], md = s[3];
+            // row max: eight independent chains of 3-input max
+            float mc[8];
 #pragma unroll
-            for (int i = 4; i < 124; i += 8) {
-                ma = max3(ma, s[i], s[i + 1]);
-                mb = max3(mb, s[i + 2], s[i + 3]);
-                mc = max3(mc, s[i + 4], s[i + 5]);
-                md = max3(md, s[i + 6], s[i + 7]);
-            }
-            ma = max3(ma, s[124], s[125]);
-            mb = max3(mb, s[126], s[127]);
-            const float mx = max3(ma, mb, fmaxf(mc, md)) * sc;
+            for (int c = 0; c < 8; ++c) mc[c] = max3(s[c], s[8 + 2 * c], s[9 + 2 * c]);
+#pragma unroll
+            for (int i = 24; i < 128; i += 16)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) mc[c] = max3(mc[c], s[i + 2 * c], s[i + 2 * c + 1]);
+            const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sc;
             // keep the stale max unless the new one exceeds it by the slack
             const float mnew = (mx > m + ATT_RESCALE_LOG2) ? mx : m;
             if (j > 0 && __any_sync(0xffffffffu, mnew != m)) {
@@ -372,14 +367,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
                 l *= alpha;
             }
             m = mnew;
-            // masked tiles hold -inf scores: they take the exact ex2 path throughout
-            const float sum = full ? softmax_exp_store<FLUX3_ATT_POLY_EVERY>(s, sc, m, tS)
-                                   : softmax_exp_store<0>(s, sc, m, tS);
-            l += sum;
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(t));
+            // P in two halves (keys 0..63, then 64..127), each signalled as soon as it is in
+            // TMEM.  Masked tiles hold -inf scores: they take the exact ex2 path throughout.
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                l += full ? softmax_exp_store<FLUX3_ATT_POLY_EVERY>(s, h, sc, m, tS)
+                          : softmax_exp_store<0>(s, h, sc, m, tS);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(h == 0 ? p_half(t) : p_full(t));
+            }
         }
         if (ok && mbar_wait_warp(o_full(t), 0, abort_flag)) {
             tc_fence_after();

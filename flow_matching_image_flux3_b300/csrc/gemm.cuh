@@ -387,22 +387,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 if (!mbar_wait_warp(full_bar(s), ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                if (leader) {
-                    const uint32_t sa = smem_base + s * C::STAGE_BYTES;
-                    const uint64_t ad = sdesc_kmajor_sw128(sa);
-                    const uint64_t bd = sdesc_kmajor_sw128(sa + C::A_BYTES);
+                const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+                const uint64_t ad = sdesc_kmajor_sw128(sa);
+                const uint64_t bd = sdesc_kmajor_sw128(sa + C::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < GEMM_BK / 16; ++k)
-                        mma_bf16_ss(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
-                    if (CL == 2) mma_commit_multicast(empty_bar(s), kPair);
-                    else mma_commit(empty_bar(s));
-                }
-                __syncwarp();
+                for (int k = 0; k < GEMM_BK / 16; ++k)
+                    mma_bf16_ss_if(leader, d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
+                if (CL == 2) mma_commit_multicast_if(leader, empty_bar(s), kPair);
+                else mma_commit_if(leader, empty_bar(s));
                 if (++s == C::STAGES) { s = 0; ph ^= 1u; }
             }
             if (!ok) break;
-            if (leader) mma_commit(tfull_bar(acc));
-            __syncwarp();
+            mma_commit_if(leader, tfull_bar(acc));
             if (++acc == 2) { acc = 0; aph ^= 1u; }
         }
         // all issued MMAs retire before TMEM is released

@@ -190,6 +190,44 @@ F3_DEV void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
                  : "memory");
 }
 
+// Warp-uniform forms: executed by a whole converged warp, the operation is performed by
+// the lanes with `issue` set (one elected lane) through a predicate instead of a branch, so
+// the warp never splits into a divergent region around it.
+F3_DEV void mma_bf16_ss_if(bool issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"((uint32_t)issue)
+        : "memory");
+}
+F3_DEV void mma_bf16_ts_if(bool issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"((uint32_t)issue)
+        : "memory");
+}
+F3_DEV void mma_commit_if(bool issue, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"((uint32_t)issue)
+        : "memory");
+}
+F3_DEV void mma_commit_multicast_if(bool issue, uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %2, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+        "h"(cta_mask), "r"((uint32_t)issue)
+        : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32*(w%4)..).
 F3_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
