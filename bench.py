@@ -36,6 +36,11 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", choices=["joint", "stage1", "joint_ref", "dit", "loop"], default="joint",
+                   help="joint: the headline 4,256-token joint block.  The others print one line each for "
+                        "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
+                        "(4096+4096+160 tokens), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
+                        "loop (50 sampling steps of dit + Euler update)")
     return p.parse_args()
 
 
@@ -49,8 +54,8 @@ def block_flops(D, F, n):
 # DRAM traffic of one in_proj launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
 # ncu capture summarised in profiles/joint_block_4256_ncu_full.md; reported only while the
 # kernel sources are the ones that capture measured.
-IN_PROJ_TRAFFIC_BYTES = (199.0 + 138.1) * 1e6
-IN_PROJ_SOURCES = {"gemm.cuh": "d175a4c52a776cf1", "sm103.cuh": "93930c071c5bf73e"}
+IN_PROJ_TRAFFIC_BYTES = (203.685376 + 140.628224) * 1e6
+IN_PROJ_SOURCES = {"gemm.cuh": "7900b66b31a42051", "sm103.cuh": "b44b224cb54cb3df", "flux3.cu": "dc91de8912b1118c"}
 
 
 def in_proj_traffic():
@@ -388,10 +393,147 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _timed(fn, steps, warmup, stream):
+    """Device time of `steps` calls of fn (after `warmup`), CUDA events on the launching stream."""
+    import torch
+    for _ in range(max(warmup, 3)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_workload(args):
+    """The other workloads, one JSON line each (not the headline line)."""
+    import torch
+    from flow_matching_image_flux3_b300 import build as fbuild
+    fbuild.build()
+    from flow_matching_image_flux3_b300 import binding as B, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    out = {"impl": "ours", "workload": args.workload, "n_gpus": 1, "data": "synthetic", "dtype": "bf16",
+           "higher_is_better": True, "unit": "tokens/s"}
+    if args.workload in ("stage1", "joint_ref"):
+        case = synth.config(2 if args.workload == "stage1" else 3)
+        d, N = case.dims, case.n
+        D, F = d.width, d.ffn_hidden
+
+        class DW:
+            def __init__(self, w):
+                self.w_in, self.b_in = w.w_in.to(dev), None
+                self.q_norm, self.k_norm = w.q_norm.to(dev), w.k_norm.to(dev)
+                self.w_out, self.b_out = w.w_out.to(dev), None
+        ws_ = [DW(w) for w in case.weights]
+        x, mod, pos = case.x.to(dev), case.mod.to(dev), case.pos.to(dev)
+        rope = torch.empty(N, 64, 2, dtype=torch.float32, device=dev)
+        x_out = torch.empty_like(x)
+        wsp = B.workspace(B.block_workspace_size(d, N), dev)
+
+        def step():
+            B.rope_build(d, pos, out=rope, stream=stream)
+            if case.stage == 1:
+                B.stream_block_fwd(d, ws_, case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
+            else:
+                B.block_fwd(d, ws_[0], case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
+        ms = _timed(step, args.steps, args.warmup, stream)
+        segs = [case.seg_off[i + 1] - case.seg_off[i] for i in range(len(case.seg_off) - 1)]
+        g1, _, g2 = block_flops(D, F, N)
+        at = sum(4.0 * n * n * D for n in segs) if case.stage == 1 else 4.0 * N * N * D
+        flops = g1 + at + g2
+        with B.Profile(capacity=16 * 20) as prof:
+            for _ in range(20):
+                step()
+        per = {}
+        for name, t in prof.records:
+            per.setdefault(name, []).append(t)
+        out.update({"metric": f"{args.workload} block tokens/s", "value": N / (ms / 1e3), "ms_per_step": ms,
+                    "tflops": flops / (ms / 1e3) / 1e12, "steps": args.steps, "warmup": args.warmup,
+                    "config": {"tokens": N, "segments": segs, "stage": case.stage, "flops_per_step": flops},
+                    "kernels_avg_ms": {k: sum(v) / len(v) for k, v in per.items()}})
+    else:
+        # the denoiser: 5 stage-1 blocks (image | text, own weights each), 28 joint blocks, output
+        # layer 3072 -> 128 on image rows; 1024x1024 text-to-image: 4,096 image + 160 text tokens.
+        # Weights ~ N(0, 1/fan_in) drawn on the device (seeded); 9.3 GB.
+        d = synth.FULL
+        D, F, H = d.width, d.ffn_hidden, d.heads
+        n_img, n_txt = 4096, 160
+        N = n_img + n_txt
+        g = torch.Generator(device=dev).manual_seed(4)
+
+        def rnd(shape, std, dtype=torch.bfloat16):
+            return (torch.randn(*shape, generator=g, device=dev) * std).to(dtype)
+
+        class DW:
+            def __init__(self):
+                self.w_in, self.b_in = rnd((3 * D + 2 * F, D), D ** -0.5), None
+                self.q_norm = 1 + rnd((128,), 0.1, torch.float32)
+                self.k_norm = 1 + rnd((128,), 0.1, torch.float32)
+                self.w_out, self.b_out = rnd((D, D + F), (D + F) ** -0.5), None
+        n_s1, n_j = 5, 28
+        stage1 = [[DW(), DW()] for _ in range(n_s1)]
+        joint = [DW() for _ in range(n_j)]
+        w_final = rnd((128, D), D ** -0.5)
+
+        def mods():
+            def m(*lead):
+                t = torch.empty(*lead, 3, D, device=dev)
+                t[..., 0:2, :].normal_(0, 0.1, generator=g)
+                t[..., 2, :].normal_(0, 0.5, generator=g)
+                return t
+            fin = torch.empty(2, D, device=dev).normal_(0, 0.1, generator=g)
+            return m(n_s1, 2), m(n_j, 2), fin
+        n_sets = 50 if args.workload == "loop" else 1
+        dargs = [B.DitArgs(stage1, joint, w_final, None, *mods(), 2) for _ in range(n_sets)]
+        streams = [synth.image_stream(1024, 1024), synth.text_stream(n_txt)]
+        pos = synth.positions(streams).to(dev)
+        base = rnd((N, D), 1.0)
+        tok = torch.empty_like(base)
+        vel = torch.empty(n_img, 128, dtype=torch.float32, device=dev)
+        wsp = B.workspace(B.dit_workspace_size(d, n_img, 0, n_txt), dev)
+        latent = torch.randn(n_img, 128, generator=g, device=dev)
+        sig = torch.sort(torch.rand(49, generator=torch.Generator().manual_seed(4)), descending=True).values.tolist()
+        sigmas = [1.0] + sig + [0.0]
+        fwd_flops = n_s1 * (sum(block_flops(D, F, n)[0] + block_flops(D, F, n)[2] + 4.0 * n * n * D
+                                for n in (n_img, n_txt))) + n_j * sum(block_flops(D, F, N)) + 2.0 * n_img * D * 128
+
+        def forward(i=0):
+            tok.copy_(base)  # the stack works in place on the token buffer
+            B.dit_fwd(d, dargs[i], tok, n_img, 0, n_txt, pos, velocity=vel, ws=wsp, stream=stream)
+
+        if args.workload == "dit":
+            ms = _timed(forward, args.steps, args.warmup, stream)
+            out.update({"metric": "denoiser forward tokens/s (1024x1024 T2I, 4256 tokens)", "value": N / (ms / 1e3),
+                        "ms_per_forward": ms, "tflops": fwd_flops / (ms / 1e3) / 1e12, "steps": args.steps,
+                        "warmup": args.warmup,
+                        "config": {"tokens": N, "stage1_blocks": n_s1, "joint_blocks": n_j, "flops_per_forward": fwd_flops,
+                                   "weights_gb": (n_s1 * 2 + n_j) * (3 * D + 2 * F + D + F) * D * 2 / 1e9}})
+        else:
+            def loop():
+                for i in range(50):
+                    forward(i)
+                    B.euler_step(latent, vel, sigmas[i], sigmas[i + 1], stream=stream)
+            ms = _timed(loop, max(1, args.steps), 1, stream)
+            out.update({"metric": "50-step sampling loop, images/s (1024x1024)", "value": 1e3 / ms, "unit": "images/s",
+                        "ms_per_image": ms, "tflops": 50 * fwd_flops / (ms / 1e3) / 1e12, "steps": max(1, args.steps),
+                        "config": {"tokens": N, "steps_per_image": 50, "flops_per_image": 50 * fwd_flops,
+                                   "note": "token buffer reset from a fixed embedding each step (the embedders "
+                                           "are not part of this path)"}})
+    assert B.device_error() == 0
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "joint":
+        run_workload(args)
     else:
         run_ours(args)
 
