@@ -61,50 +61,84 @@ __global__ void rope_table_kernel(const int* __restrict__ pos, int n_tokens, con
 // Nothing of the row stays in registers, so 32 warps fit on an SM and a 4,256-row call has
 // every row in flight in one wave.  A block's 8 rows nearly always share one segment: its
 // shift and scale vectors are then staged once in shared memory (instead of every warp
-// streaming 2 D floats through L1 per row).
+// streaming 2 D floats through L1 per row).  The arithmetic runs on packed fp32 pairs.
 constexpr int kAdaLnMaxChunks = 16;  // D <= 4096
 
-F3_DEV void unpack_bf16x8(const uint4& u, float (&f)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        f[2 * e] = __uint_as_float(w[e] << 16);
-        f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    }
+
+// fp32 pairs in one 64-bit register for the packed f32x2 instructions (two fp32
+// operations per issue slot)
+F3_DEV uint64_t ln_f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
+F3_DEV void ln_split(uint64_t v, float& lo, float& hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
+F3_DEV uint64_t ln_fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+F3_DEV uint64_t ln_add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+F3_DEV uint64_t ln_mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16 pair (low half = lower column) -> fp32 pair
+F3_DEV uint64_t ln_bf2(uint32_t w) { return ln_f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
 
 template <int NC>
 __global__ void __launch_bounds__(256, 4) adaln_kernel(const __nv_bfloat16* __restrict__ x, int n_rows, float eps,
                                                     const float* __restrict__ mod, const __grid_constant__ SegOffsets segs,
                                                     __nv_bfloat16* __restrict__ a) {
     constexpr int D = NC * 256;
-    __shared__ __align__(16) float s_mod[2 * D];  // shift | scale of the block's segment
+    // the block's segment's (1 + scale) and shift, laid out so that the float4 a lane needs
+    // for its 8 columns sits next to its neighbours' (conflict-free): index
+    // ((chunk * 2 + half) * 32 + lane) * 4 holds columns chunk * 256 + lane * 8 + half * 4 ..
+    __shared__ __align__(16) float s_scale1[D], s_shift[D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r_first = blockIdx.x * 8;
     const int r_last = min(r_first + 7, n_rows - 1);
     const int seg_first = segment_of_row(segs, r_first);
     const bool staged = segment_of_row(segs, r_last) == seg_first;  // uniform over the block
     if (staged) {
-        const float4* src = reinterpret_cast<const float4*>(mod + (size_t)seg_first * 3 * D);
-        for (int i = threadIdx.x; i < 2 * D / 4; i += blockDim.x) reinterpret_cast<float4*>(s_mod)[i] = __ldg(src + i);
+        const float4* sh4 = reinterpret_cast<const float4*>(mod + (size_t)seg_first * 3 * D);
+        const float4* sc4 = sh4 + D / 4;
+        for (int i = threadIdx.x; i < D / 4; i += blockDim.x) {
+            const int col = 4 * i, c = col >> 8, ln = (col & 255) >> 3, hf = (col >> 2) & 1;
+            const int dst = ((c * 2 + hf) * 32 + ln) * 4;
+            float4 v = __ldg(sc4 + i);
+            v.x += 1.f; v.y += 1.f; v.z += 1.f; v.w += 1.f;
+            *reinterpret_cast<float4*>(s_scale1 + dst) = v;
+            *reinterpret_cast<float4*>(s_shift + dst) = __ldg(sh4 + i);
+        }
         __syncthreads();
     }
     const int r = r_first + warp;
     if (r >= n_rows) return;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * D);
     const float c0 = __bfloat162float(x[(size_t)r * D]);
-    float sum = 0.f, sq = 0.f;
+    const uint64_t c02 = ln_f2(-c0, -c0);
+    uint64_t sum2 = 0, sq2 = 0;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        float f[8];
-        unpack_bf16x8(__ldg(xr + c * 32 + lane), f);
+        const uint4 u = __ldg(xr + c * 32 + lane);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float d = f[e] - c0;
-            sum += d;
-            sq = fmaf(d, d, sq);
+        for (int e = 0; e < 4; ++e) {
+            const uint64_t d = ln_add2(ln_bf2(w[e]), c02);
+            sum2 = ln_add2(sum2, d);
+            sq2 = ln_fma2(d, d, sq2);
         }
     }
+    float s0, s1, q0, q1;
+    ln_split(sum2, s0, s1);
+    ln_split(sq2, q0, q1);
+    float sum = s0 + s1, sq = q0 + q1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -113,23 +147,44 @@ __global__ void __launch_bounds__(256, 4) adaln_kernel(const __nv_bfloat16* __re
     const float md = sum * (1.f / D);
     const float mean = c0 + md;
     const float rstd = rsqrtf(fmaxf(sq * (1.f / D) - md * md, 0.f) + eps);
-    const float* shift = staged ? s_mod : mod + (size_t)segment_of_row(segs, r) * 3 * D;
-    const float* scale = shift + D;
+    // a = x * A + B with A = rstd * (1 + scale), B = shift - mean * A
+    const uint64_t rstd2 = ln_f2(rstd, rstd), nmean2 = ln_f2(-mean, -mean);
+    const float* gshift = mod + (size_t)segment_of_row(segs, r) * 3 * D;
     uint4* ar = reinterpret_cast<uint4*>(a + (size_t)r * D);
-#pragma unroll 2
+#pragma unroll 1
     for (int c = 0; c < NC; ++c) {
-        const int col = c * 256 + lane * 8;
-        const float4 s0 = *reinterpret_cast<const float4*>(scale + col);
-        const float4 s1 = *reinterpret_cast<const float4*>(scale + col + 4);
-        const float4 h0 = *reinterpret_cast<const float4*>(shift + col);
-        const float4 h1 = *reinterpret_cast<const float4*>(shift + col + 4);
-        float f[8];
-        unpack_bf16x8(__ldg(xr + c * 32 + lane), f);
-        auto mo = [&](float v, float sc, float sh) { return fmaf((v - mean) * rstd, 1.f + sc, sh); };
-        ar[c * 32 + lane] = make_uint4(pack_bf16(mo(f[0], s0.x, h0.x), mo(f[1], s0.y, h0.y)),
-                                       pack_bf16(mo(f[2], s0.z, h0.z), mo(f[3], s0.w, h0.w)),
-                                       pack_bf16(mo(f[4], s1.x, h1.x), mo(f[5], s1.y, h1.y)),
-                                       pack_bf16(mo(f[6], s1.z, h1.z), mo(f[7], s1.w, h1.w)));
+        float4 s1v[2], shv[2];
+        if (staged) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                s1v[hf] = *reinterpret_cast<const float4*>(s_scale1 + ((c * 2 + hf) * 32 + lane) * 4);
+                shv[hf] = *reinterpret_cast<const float4*>(s_shift + ((c * 2 + hf) * 32 + lane) * 4);
+            }
+        } else {
+            const int col = c * 256 + lane * 8;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                s1v[hf] = __ldg(reinterpret_cast<const float4*>(gshift + D + col + 4 * hf));
+                s1v[hf].x += 1.f; s1v[hf].y += 1.f; s1v[hf].z += 1.f; s1v[hf].w += 1.f;
+                shv[hf] = __ldg(reinterpret_cast<const float4*>(gshift + col + 4 * hf));
+            }
+        }
+        const uint4 u = __ldg(xr + c * 32 + lane);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4& sv = s1v[e >> 1];
+            const float4& hv = shv[e >> 1];
+            const uint64_t sc2 = (e & 1) ? ln_f2(sv.z, sv.w) : ln_f2(sv.x, sv.y);
+            const uint64_t sh2 = (e & 1) ? ln_f2(hv.z, hv.w) : ln_f2(hv.x, hv.y);
+            const uint64_t A = ln_mul2(rstd2, sc2);
+            const uint64_t Bv = ln_fma2(nmean2, A, sh2);
+            float y0, y1;
+            ln_split(ln_fma2(ln_bf2(w[e]), A, Bv), y0, y1);
+            o[e] = pack_bf16(y0, y1);
+        }
+        ar[c * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
