@@ -19,7 +19,8 @@ c_i32, c_f32, c_vp, c_size = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ct
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 MAX_SEGMENTS = 16
-KERNEL_NAMES = {1: "rope", 2: "adaln", 3: "in_proj", 4: "attn", 5: "out_proj", 6: "final", 7: "euler", 8: "attn_f32"}
+KERNEL_NAMES = {1: "rope", 2: "adaln", 3: "in_proj", 4: "attn", 5: "out_proj", 6: "final", 7: "euler", 8: "attn_f32",
+                9: "linear", 10: "cfg_euler", 11: "to_bf16"}
 
 
 class flux3_dims(ctypes.Structure):
@@ -43,6 +44,13 @@ class flux3_dit_weights(ctypes.Structure):
 
 class flux3_dit_mod(ctypes.Structure):
     _fields_ = [("stage1", c_vp), ("joint", c_vp), ("final", c_vp)]
+
+
+class flux3_sample_args(ctypes.Structure):
+    _fields_ = [("n_img", c_i32), ("n_ref", c_i32), ("n_txt", c_i32), ("latent_channels", c_i32), ("text_dim", c_i32),
+                ("w_img", c_vp), ("b_img", c_vp), ("w_txt", c_vp), ("b_txt", c_vp), ("ref_latent", c_vp),
+                ("text_pos", c_vp), ("text_neg", c_vp), ("pos", c_vp), ("mod", ctypes.POINTER(flux3_dit_mod)),
+                ("n_steps", c_i32), ("alpha", c_f32), ("cfg_scale", c_f32)]
 
 
 class Flux3Error(RuntimeError):
@@ -78,6 +86,12 @@ def _load() -> ctypes.CDLL:
         "flux3_dit_fwd": (c_i32, [P(flux3_dims), P(flux3_dit_weights), P(flux3_dit_mod), c_vp, c_i32, c_i32, c_i32,
                                   c_vp, c_vp, c_vp, c_size, c_vp]),
         "flux3_euler_step": (c_i32, [c_vp, c_vp, ctypes.c_int64, c_f32, c_f32, c_vp]),
+        "flux3_sigma_schedule": (c_i32, [c_i32, c_f32, P(c_f32)]),
+        "flux3_linear_fwd": (c_i32, [P(flux3_dims), c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp]),
+        "flux3_cfg_euler_step": (c_i32, [c_vp, c_vp, c_vp, ctypes.c_int64, c_f32, c_f32, c_f32, c_vp, c_vp]),
+        "flux3_sample_workspace_size": (c_size, [P(flux3_dims), P(flux3_sample_args)]),
+        "flux3_sample_fwd": (c_i32, [P(flux3_dims), P(flux3_dit_weights), P(flux3_sample_args), c_vp, c_vp, c_size,
+                                     c_vp]),
         "flux3_block_fwd_static": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp,
                                            c_i32, c_vp, c_vp]),
         "flux3_device_error": (c_i32, [P(ctypes.c_uint32), c_i32]),
@@ -97,6 +111,8 @@ EXPORTED = [
     "flux3_attn_fwd", "flux3_out_proj_fwd", "flux3_block_workspace_size", "flux3_block_fwd",
     "flux3_stream_block_fwd", "flux3_final_fwd", "flux3_dit_workspace_size", "flux3_dit_fwd", "flux3_euler_step",
     "flux3_device_error", "flux3_profile_begin", "flux3_profile_end", "flux3_block_fwd_static",
+    "flux3_sigma_schedule", "flux3_linear_fwd", "flux3_cfg_euler_step", "flux3_sample_workspace_size",
+    "flux3_sample_fwd",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -332,6 +348,71 @@ def dit_fwd(dims, args: DitArgs, tokens: torch.Tensor, n_img: int, n_ref: int, n
 def euler_step(latent: torch.Tensor, velocity: torch.Tensor, sigma: float, sigma_next: float, stream=None) -> None:
     _check("flux3_euler_step", lib.flux3_euler_step(_ptr(latent, torch.float32), _ptr(velocity, torch.float32),
                                                     latent.numel(), sigma, sigma_next, _stream(stream)))
+
+
+def sigma_schedule(n_steps: int, alpha: float) -> List[float]:
+    """Noise levels of an n_steps run (host only, no GPU needed)."""
+    out = (c_f32 * (n_steps + 1))()
+    _check("flux3_sigma_schedule", lib.flux3_sigma_schedule(n_steps, alpha, out))
+    return list(out)
+
+
+def linear_fwd(dims, x: torch.Tensor, w: torch.Tensor, b: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[r, :D] = x[r] W^T + b in bf16 (a token embedder); out may be a row slice of a
+    wider token buffer (its row stride is passed)."""
+    rows, k = x.shape
+    out = out if out is not None else torch.empty(rows, dims.width, dtype=torch.bfloat16, device=x.device)
+    assert out.dtype == torch.bfloat16 and out.stride(1) == 1 and out.shape[0] == rows
+    d = make_dims(dims)
+    if not out.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    _check("flux3_linear_fwd", lib.flux3_linear_fwd(ctypes.byref(d), _ptr(x, torch.bfloat16), rows, k,
+                                                    _ptr(w, torch.bfloat16), _ptr(b, torch.float32), out.data_ptr(),
+                                                    out.stride(0), _stream(stream)))
+    return out
+
+
+def cfg_euler_step(latent: torch.Tensor, v_pos: torch.Tensor, v_neg: Optional[torch.Tensor], cfg_scale: float,
+                   sigma: float, sigma_next: float, latent_bf16: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check("flux3_cfg_euler_step", lib.flux3_cfg_euler_step(
+        _ptr(latent, torch.float32), _ptr(v_pos, torch.float32), _ptr(v_neg, torch.float32), latent.numel(),
+        cfg_scale, sigma, sigma_next, _ptr(latent_bf16, torch.bfloat16), _stream(stream)))
+
+
+class SampleArgs:
+    """Host struct of the sampling loop; keeps the tensors and the per-step modulation
+    structs alive."""
+
+    def __init__(self, n_img: int, n_ref: int, n_txt: int, w_img: torch.Tensor, b_img: Optional[torch.Tensor],
+                 w_txt: torch.Tensor, b_txt: Optional[torch.Tensor], text_pos: torch.Tensor,
+                 text_neg: Optional[torch.Tensor], pos: torch.Tensor, step_mods: Sequence, n_steps: int,
+                 alpha: float, cfg_scale: float, ref_latent: Optional[torch.Tensor] = None):
+        # step_mods: one (mod_stage1, mod_joint, mod_final) device tuple per step
+        self._keep = [w_img, b_img, w_txt, b_txt, text_pos, text_neg, pos, step_mods, ref_latent]
+        self.mods = (flux3_dit_mod * n_steps)(*[flux3_dit_mod(_ptr(m[0], torch.float32), _ptr(m[1], torch.float32),
+                                                             _ptr(m[2], torch.float32)) for m in step_mods])
+        self.a = flux3_sample_args(n_img, n_ref, n_txt, w_img.shape[1], w_txt.shape[1], _ptr(w_img, torch.bfloat16),
+                                   _ptr(b_img, torch.float32), _ptr(w_txt, torch.bfloat16), _ptr(b_txt, torch.float32),
+                                   _ptr(ref_latent, torch.bfloat16), _ptr(text_pos, torch.bfloat16),
+                                   _ptr(text_neg, torch.bfloat16), _ptr(pos, torch.int32),
+                                   ctypes.cast(self.mods, ctypes.POINTER(flux3_dit_mod)), n_steps, alpha, cfg_scale)
+
+
+def sample_workspace_size(dims, args: SampleArgs) -> int:
+    d = make_dims(dims)
+    return int(lib.flux3_sample_workspace_size(ctypes.byref(d), ctypes.byref(args.a)))
+
+
+def sample_fwd(dims, dit: "DitArgs", args: SampleArgs, latent: torch.Tensor, ws: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Runs the sampling loop in place on latent (fp32 [n_img, latent_channels])."""
+    ws = ws if ws is not None else workspace(sample_workspace_size(dims, args), latent.device)
+    d = make_dims(dims)
+    _check("flux3_sample_fwd", lib.flux3_sample_fwd(ctypes.byref(d), ctypes.byref(dit.w), ctypes.byref(args.a),
+                                                    _ptr(latent, torch.float32), _ptr(ws), ws.numel(),
+                                                    _stream(stream)))
+    return latent
 
 
 def device_error(reset: bool = True) -> int:

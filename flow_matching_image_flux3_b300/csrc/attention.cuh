@@ -116,7 +116,7 @@ F3_DEV float softmax_exp_store(const float (&s)[128], int h, float sc, float m, 
             const int e = 64 * h + 2 * i;
             float x0, x1, p0, p1;
             f2_split(f2_fma(f2(s[e], s[e + 1]), sc2, nm2), x0, x1);
-            if (POLY > 0 && (i % POLY) == POLY - 1) {
+            if (POLY > 0 && (i % (POLY > 0 ? POLY : 1)) == POLY - 1) {
                 exp2_poly2(x0, x1, p0, p1);
             } else {
                 p0 = ex2(x0);

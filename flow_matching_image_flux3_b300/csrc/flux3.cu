@@ -403,6 +403,75 @@ flux3_status run_final(const flux3_dims* d, const void* w_final, const float* b_
     return launch_gemm<128, EPI_F32, 1>(P, st, FLUX3_KERNEL_FINAL);
 }
 
+flux3_status run_linear(const flux3_dims* d, const void* x, int rows, int k, const void* w, const float* b, void* out,
+                        int ld_out, cudaStream_t st) {
+    if (rows == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    const int D = d->width;
+    if (!tmap_2d(&P.tm_a, x, k, rows, (uint64_t)k * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_2d(&P.tm_b[0], w, k, D, (uint64_t)k * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    P.ew[0] = {b, nullptr, nullptr};
+    const int32_t off[2] = {0, rows};
+    fill_groups(P, off, 1, 1, rows, 1);
+    P.n_tiles = D / 256;
+    P.k_blocks = k / GEMM_BK;
+    P.width = D;
+    P.out_bf = static_cast<__nv_bfloat16*>(out);
+    P.ld_out = ld_out;
+    return launch_gemm<256, EPI_BF16, 1>(P, st, FLUX3_KERNEL_LINEAR);
+}
+
+flux3_status run_cfg_euler(float* latent, const float* vp, const float* vn, long long n, float s, float dt,
+                           __nv_bfloat16* lat_bf, cudaStream_t st) {
+    if (n == 0) return FLUX3_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return FLUX3_ERR_CUDA;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    prof_before(FLUX3_KERNEL_CFG_EULER, st);
+    cfg_euler_kernel<<<(unsigned)blocks, 256, 0, st>>>(latent, vp, vn, n, s, dt, lat_bf);
+    prof_after(st);
+    return launch_status();
+}
+
+void sigma_schedule(int n_steps, double alpha, float* out) {
+    for (int i = 0; i <= n_steps; ++i) {
+        const double x = 1.0 - (double)i / n_steps;
+        out[i] = (float)(alpha * x / (1.0 + (alpha - 1.0) * x));
+    }
+}
+
+// workspace of the sampling loop: tokens | reference+text context (prompt) | context
+// (negative prompt, with guidance) | latent in bf16 | velocities | the denoiser's workspace
+struct SampleWs {
+    __nv_bfloat16 *tokens, *ctx_pos, *ctx_neg, *lat_bf;
+    float *v_pos, *v_neg;
+    uint8_t* dit;
+    size_t dit_bytes, bytes;
+};
+SampleWs sample_ws_layout(const flux3_dims* d, const flux3_sample_args* a, uint8_t* base) {
+    SampleWs w;
+    const size_t D = d->width, N = (size_t)a->n_img + a->n_ref + a->n_txt, nc = (size_t)a->n_ref + a->n_txt;
+    const bool cfg = a->cfg_scale != 1.f;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? base + off : nullptr;
+        off += up256(bytes);
+        return p;
+    };
+    w.tokens = reinterpret_cast<__nv_bfloat16*>(take(N * D * 2));
+    w.ctx_pos = reinterpret_cast<__nv_bfloat16*>(take(nc * D * 2));
+    w.ctx_neg = cfg ? reinterpret_cast<__nv_bfloat16*>(take(nc * D * 2)) : nullptr;
+    w.lat_bf = reinterpret_cast<__nv_bfloat16*>(take((size_t)a->n_img * a->latent_channels * 2));
+    w.v_pos = reinterpret_cast<float*>(take((size_t)a->n_img * a->latent_channels * 4));
+    w.v_neg = cfg ? reinterpret_cast<float*>(take((size_t)a->n_img * a->latent_channels * 4)) : nullptr;
+    w.dit_bytes = flux3_dit_workspace_size(d, a->n_img, a->n_ref, a->n_txt);
+    w.dit = take(w.dit_bytes);
+    w.bytes = off;
+    return w;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- static scratch
@@ -649,6 +718,107 @@ flux3_status flux3_euler_step(float* latent, const float* velocity, int64_t n, f
     euler_kernel<<<(unsigned)blocks, 256, 0, st>>>(latent, velocity, n, sigma_next - sigma);
     prof_after(st);
     return launch_status();
+}
+
+flux3_status flux3_sigma_schedule(int32_t n_steps, float alpha, float* sigmas) {
+    if (n_steps < 1 || !sigmas || !(alpha > 0.f) || !std::isfinite(alpha)) return FLUX3_ERR_INVALID_ARG;
+    sigma_schedule(n_steps, alpha, sigmas);
+    return FLUX3_OK;
+}
+
+flux3_status flux3_linear_fwd(const flux3_dims* dims, const void* x, int32_t rows, int32_t k, const void* w, const float* b,
+                              void* out, int32_t ld_out, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (rows < 0 || rows > kMaxTokens || k <= 0 || k > (1 << 20)) return FLUX3_ERR_INVALID_ARG;
+    if (k % GEMM_BK != 0 || dims->width % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (rows == 0) return FLUX3_OK;
+    if (!x || !w || !out || !al16(x) || !al16(w) || !al16(out) || (b && !al16(b))) return FLUX3_ERR_INVALID_ARG;
+    if (ld_out < dims->width || ld_out % 8 != 0) return FLUX3_ERR_INVALID_ARG;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    return run_linear(dims, x, rows, k, w, b, out, ld_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_cfg_euler_step(float* latent, const float* v_pos, const float* v_neg, int64_t n, float cfg_scale,
+                                  float sigma, float sigma_next, void* latent_bf16, flux3_stream_t stream) {
+    if (n < 0 || (n > 0 && (!latent || !v_pos))) return FLUX3_ERR_INVALID_ARG;
+    if (!std::isfinite(cfg_scale) || !std::isfinite(sigma) || !std::isfinite(sigma_next)) return FLUX3_ERR_INVALID_ARG;
+    return run_cfg_euler(latent, v_pos, v_neg, n, cfg_scale, sigma_next - sigma, static_cast<__nv_bfloat16*>(latent_bf16),
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+static flux3_status check_sample_args(const flux3_dims* d, const flux3_sample_args* a) {
+    flux3_status s = check_dims(d);
+    if (s != FLUX3_OK) return s;
+    if (!a || a->n_img < 0 || a->n_ref < 0 || a->n_txt < 0 || a->n_steps < 1 || a->n_steps > 100000) return FLUX3_ERR_INVALID_ARG;
+    if ((long long)a->n_img + a->n_ref + a->n_txt > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if (!(a->alpha > 0.f) || !std::isfinite(a->alpha) || !std::isfinite(a->cfg_scale)) return FLUX3_ERR_INVALID_ARG;
+    if (a->latent_channels <= 0 || a->text_dim <= 0 || a->text_dim > (1 << 20) || a->latent_channels > 4096)
+        return FLUX3_ERR_INVALID_ARG;
+    if (a->latent_channels % GEMM_BK != 0 || a->text_dim % GEMM_BK != 0 || d->width % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (!a->w_img || !al16(a->w_img) || (a->b_img && !al16(a->b_img))) return FLUX3_ERR_INVALID_ARG;
+    if (a->n_txt > 0 && (!a->w_txt || !al16(a->w_txt) || (a->b_txt && !al16(a->b_txt)) || !a->text_pos ||
+                         !al16(a->text_pos)))
+        return FLUX3_ERR_INVALID_ARG;
+    if (a->n_txt > 0 && a->cfg_scale != 1.f && (!a->text_neg || !al16(a->text_neg))) return FLUX3_ERR_INVALID_ARG;
+    if (a->n_ref > 0 && (!a->ref_latent || !al16(a->ref_latent))) return FLUX3_ERR_INVALID_ARG;
+    if (!a->pos || !al16(a->pos) || !a->mod) return FLUX3_ERR_INVALID_ARG;
+    return FLUX3_OK;
+}
+
+size_t flux3_sample_workspace_size(const flux3_dims* dims, const flux3_sample_args* a) {
+    if (check_sample_args(dims, a) != FLUX3_OK) return 0;
+    return sample_ws_layout(dims, a, nullptr).bytes;
+}
+
+flux3_status flux3_sample_fwd(const flux3_dims* dims, const flux3_dit_weights* w, const flux3_sample_args* a, float* latent,
+                              void* ws, size_t ws_bytes, flux3_stream_t stream) {
+    flux3_status s = check_sample_args(dims, a);
+    if (s != FLUX3_OK) return s;
+    if (!w || w->out_channels != a->latent_channels) return FLUX3_ERR_INVALID_ARG;
+    if (w->n_streams != (a->n_ref > 0 ? 3 : 2)) return FLUX3_ERR_INVALID_ARG;
+    if (a->n_img == 0) return FLUX3_OK;
+    if (!latent || !al16(latent)) return FLUX3_ERR_INVALID_ARG;
+    const SampleWs need = sample_ws_layout(dims, a, nullptr);
+    if (!ws || !al256(ws) || ws_bytes < need.bytes) return FLUX3_ERR_WORKSPACE;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const SampleWs b = sample_ws_layout(dims, a, static_cast<uint8_t*>(ws));
+    const int D = dims->width, C = a->latent_channels;
+    const bool cfg = a->cfg_scale != 1.f;
+    const long long n_lat = (long long)a->n_img * C;
+    const size_t ctx_bytes = ((size_t)a->n_ref + a->n_txt) * D * 2;
+    std::vector<float> sig(a->n_steps + 1);
+    sigma_schedule(a->n_steps, a->alpha, sig.data());
+    // the clean context (references, text) is embedded once
+    for (int k = 0; k < (cfg ? 2 : 1); ++k) {
+        __nv_bfloat16* ctx = k == 0 ? b.ctx_pos : b.ctx_neg;
+        if ((s = run_linear(dims, a->ref_latent, a->n_ref, C, a->w_img, a->b_img, ctx, D, st)) != FLUX3_OK) return s;
+        if ((s = run_linear(dims, k == 0 ? a->text_pos : a->text_neg, a->n_txt, a->text_dim, a->w_txt, a->b_txt,
+                            ctx + (size_t)a->n_ref * D, D, st)) != FLUX3_OK)
+            return s;
+    }
+    prof_before(FLUX3_KERNEL_TO_BF16, st);
+    to_bf16_kernel<<<(unsigned)((n_lat + 255) / 256), 256, 0, st>>>(latent, n_lat, b.lat_bf);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    for (int i = 0; i < a->n_steps; ++i) {
+        for (int k = 0; k < (cfg ? 2 : 1); ++k) {
+            // the denoiser overwrites the token buffer: rebuild it for every call
+            if ((s = run_linear(dims, b.lat_bf, a->n_img, C, a->w_img, a->b_img, b.tokens, D, st)) != FLUX3_OK) return s;
+            if (ctx_bytes > 0 &&
+                cudaMemcpyAsync(b.tokens + (size_t)a->n_img * D, k == 0 ? b.ctx_pos : b.ctx_neg, ctx_bytes,
+                                cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return FLUX3_ERR_CUDA;
+            if ((s = flux3_dit_fwd(dims, w, &a->mod[i], b.tokens, a->n_img, a->n_ref, a->n_txt, a->pos,
+                                   k == 0 ? b.v_pos : b.v_neg, b.dit, b.dit_bytes, stream)) != FLUX3_OK)
+                return s;
+        }
+        if ((s = run_cfg_euler(latent, b.v_pos, cfg ? b.v_neg : nullptr, n_lat, a->cfg_scale, sig[i + 1] - sig[i], b.lat_bf,
+                               st)) != FLUX3_OK)
+            return s;
+    }
+    return FLUX3_OK;
 }
 
 flux3_status flux3_device_error(uint32_t* flags, int32_t reset) {

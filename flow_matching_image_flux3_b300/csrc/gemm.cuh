@@ -5,6 +5,7 @@
 //                       attention and SwiGLU run in parallel on the same normalized input)
 //   EPI_GATED_RESIDUAL  output projection: x_out = x + gate_s * (acc + b_out)
 //   EPI_F32             plain fp32 store (+ bias): the output layer
+//   EPI_BF16            plain bf16 store (+ bias): the token embedders
 //
 // Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads, warp 1 issues
 // tcgen05.mma and owns the TMEM allocation (both run as converged warps with one elected
@@ -21,7 +22,7 @@ constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;  // bf16 elements per 128-byte swizzle row
 constexpr int GEMM_THREADS = 192;
 
-enum EpiKind { EPI_QKV_SWIGLU = 0, EPI_GATED_RESIDUAL = 1, EPI_F32 = 2 };
+enum EpiKind { EPI_QKV_SWIGLU = 0, EPI_GATED_RESIDUAL = 1, EPI_F32 = 2, EPI_BF16 = 3 };
 
 struct GemmGroup {
     int row_begin, row_end, tile_begin, wset;
@@ -50,8 +51,9 @@ struct GemmParams {
     const float* mod;
     int n_seg;
     int seg_off[FLUX3_MAX_SEGMENTS + 1];
-    // EPI_F32
+    // EPI_F32 / EPI_BF16
     float* out;
+    __nv_bfloat16* out_bf;
     int ld_out;
 };
 
@@ -254,6 +256,29 @@ F3_DEV void epi_f32(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
     }
 }
 
+template <int BN>
+F3_DEV void epi_bf16(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t t[32];
+        tmem_ld32(tacc + c * 32, t);
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int col = n * BN + c * 32;
+        float a[32];
+        unpack32(t, a);
+        if (w.bias) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
+        }
+        __nv_bfloat16* dst = p.out_bf + (size_t)r * p.ld_out + col;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st_global_v4(dst + 8 * i, pack_bf16(a[8 * i], a[8 * i + 1]), pack_bf16(a[8 * i + 2], a[8 * i + 3]),
+                         pack_bf16(a[8 * i + 4], a[8 * i + 5]), pack_bf16(a[8 * i + 6], a[8 * i + 7]));
+    }
+}
+
 // --------------------------------------------------------------------- the kernel
 // Tiles are numbered n-major (all m-tiles of one weight tile run together, so each weight
 // tile is read from HBM once).  With CL = 2 the kernel runs as clusters of two CTAs that
@@ -437,7 +462,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
             const EpiWeights& w = p.ew[p.grp[ti.g].wset];
             if (EPI == EPI_QKV_SWIGLU) epi_qkv(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
-            else epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else if (EPI == EPI_F32) epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));

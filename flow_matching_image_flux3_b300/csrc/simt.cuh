@@ -208,6 +208,27 @@ inline bool launch_adaln(int D, const __nv_bfloat16* x, int n_rows, float eps, c
     }
 }
 
+// ---------------------------------------------------------------- guided Euler update
+// latent += dt * (v_neg + s (v_pos - v_neg)) (v_neg == nullptr: latent += dt * v_pos); the
+// updated latent rounded to bf16 goes to lat_bf (the next step's embedder input) if given.
+__global__ void cfg_euler_kernel(float* __restrict__ latent, const float* __restrict__ vp, const float* __restrict__ vn,
+                                 long long n, float s, float dt, __nv_bfloat16* __restrict__ lat_bf) {
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (; i < n; i += stride) {
+        const float v = vn ? fmaf(s, vp[i] - vn[i], vn[i]) : vp[i];
+        const float x = fmaf(dt, v, latent[i]);
+        latent[i] = x;
+        if (lat_bf) lat_bf[i] = __float2bfloat16_rn(x);
+    }
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ src, long long n, __nv_bfloat16* __restrict__ dst) {
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (; i < n; i += stride) dst[i] = __float2bfloat16_rn(src[i]);
+}
+
 // ---------------------------------------------------------------- Euler update
 __global__ void euler_kernel(float* __restrict__ latent, const float* __restrict__ vel, long long n, float dt) {
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;

@@ -107,7 +107,8 @@ const char *flux3_version(void);
 /* ---- a1: RoPE table ("How it works": four axes t, h, w, l, 32 of the 128 dims each).
  * pos   device int32 [N, 4]: (t, h, w, l) per token.
  * rope  device fp32 [N, 64, 2]: (cos, sin) of pair p = 16 a + j (axis a, j = 0..15),
- *       angle pos[a] * theta^(-2 j / 32), computed in fp64 and rounded to fp32.
+ *       angle pos[a] * theta^(-2 j / 32), reduced modulo 2 pi (in turns, exactly split
+ *       in fp32) before sin/cos: error <= pi * 2^-24 plus sincospif's rounding.
  *       Pair p rotates head dims (2p, 2p+1).  N == 0 is a no-op. */
 flux3_status flux3_rope_build(const flux3_dims *dims, const int32_t *pos, int32_t n_tokens,
                               float *rope, flux3_stream_t stream);
@@ -229,6 +230,73 @@ flux3_status flux3_dit_fwd(const flux3_dims *dims, const flux3_dit_weights *w,
 flux3_status flux3_euler_step(float *latent, const float *velocity, int64_t n, float sigma,
                               float sigma_next, flux3_stream_t stream);
 
+/* ---- the base-model sampling loop around the denoiser.  "Welcome FLUX.3 Image Klein in
+ * Diffusers", "How it works": image tokens are the 2x2 patches of the 32-channel latents
+ * packed into 128 channels; text is a 20,480-dim stack of 8 Qwen3-VL hidden layers
+ * projected to the width; references go through the same encoder as the image; the
+ * scheduler applies a time shift of 6.93, so 44 of 50 steps run above sigma = 0.5.
+ * "What it claims": the base checkpoint runs 50 steps with classifier-free guidance.
+ * DiffSynth-Studio FLUX.3 page, pipeline arguments: alpha is the rational-shift
+ * coefficient (6.93); cfg_scale 1.0 turns guidance off, the Base examples use 3.5.
+ * Readings where the pages are silent: the unshifted grid 1 - i / n_steps; the shift
+ * s(x) = alpha x / (1 + (alpha - 1) x); a step x += (sigma_next - sigma) v (velocity
+ * from data to noise); guidance v_neg + s (v_pos - v_neg); linear embedders with bias.
+ * The timestep -> modulation map is not on the pages: every step's modulation vectors
+ * are inputs. */
+
+/* Noise levels of an n_steps run, computed on the host (no GPU needed):
+ * sigmas[i] = s(1 - i / n_steps), i = 0..n_steps, so sigmas[0] = 1 and sigmas[n_steps] = 0.
+ * sigmas  host fp32 [n_steps + 1].  n_steps >= 1, alpha > 0 and finite. */
+flux3_status flux3_sigma_schedule(int32_t n_steps, float alpha, float *sigmas);
+
+/* A token embedder: out[r, 0:D] = x[r, :] W^T + b in bf16 (image: latent_channels -> D,
+ * text: text_dim -> D), fp32 accumulation.
+ * x    device bf16 [rows, k], k % 64 == 0;  w  device bf16 [D, k];  b  device fp32 [D] or NULL.
+ * out  device bf16 rows of stride ld_out elements (ld_out >= D, ld_out % 8 == 0): typically
+ *      the rows of a token buffer. */
+flux3_status flux3_linear_fwd(const flux3_dims *dims, const void *x, int32_t rows, int32_t k, const void *w,
+                              const float *b, void *out, int32_t ld_out, flux3_stream_t stream);
+
+/* One guided Euler step: latent += (sigma_next - sigma) (v_neg + s (v_pos - v_neg)), or
+ * latent += (sigma_next - sigma) v_pos when v_neg is NULL (no guidance).
+ * latent, v_pos, v_neg  device fp32 [n].  latent_bf16: device bf16 [n] that receives the
+ * updated latent rounded to bf16 (the next step's embedder input), or NULL. */
+flux3_status flux3_cfg_euler_step(float *latent, const float *v_pos, const float *v_neg, int64_t n, float cfg_scale,
+                                  float sigma, float sigma_next, void *latent_bf16, flux3_stream_t stream);
+
+/* The sampling loop's inputs (host struct pointing at device memory). */
+typedef struct flux3_sample_args {
+    int32_t n_img, n_ref, n_txt;  /* tokens per stream; order image | reference | text          */
+    int32_t latent_channels;      /* 128: a packed 2x2 patch of 32-channel latents (% 64 == 0)  */
+    int32_t text_dim;             /* 20,480: the stacked text features (% 64 == 0)              */
+    const void *w_img;            /* device bf16 [D, latent_channels]: image/reference embedder */
+    const float *b_img;           /* device fp32 [D] or NULL                                    */
+    const void *w_txt;            /* device bf16 [D, text_dim]: text embedder                   */
+    const float *b_txt;           /* device fp32 [D] or NULL                                    */
+    const void *ref_latent;       /* device bf16 [n_ref, latent_channels] (clean) or NULL       */
+    const void *text_pos;         /* device bf16 [n_txt, text_dim]: the prompt's features       */
+    const void *text_neg;         /* device bf16 [n_txt, text_dim]: the negative prompt's;
+                                     required when cfg_scale != 1, ignored otherwise            */
+    const int32_t *pos;           /* device int32 [N, 4] position ids (N = n_img + n_ref + n_txt) */
+    const flux3_dit_mod *mod;     /* host [n_steps]: each step's modulation vectors (device)    */
+    int32_t n_steps;              /* >= 1 (50 for the base checkpoint)                          */
+    float alpha;                  /* rational time shift (6.93)                                 */
+    float cfg_scale;              /* 1 = no guidance (one denoiser call per step), else two     */
+} flux3_sample_args;
+
+/* Workspace of flux3_sample_fwd in bytes (0 for invalid arguments). */
+size_t flux3_sample_workspace_size(const flux3_dims *dims, const flux3_sample_args *a);
+
+/* The loop: for i = 0..n_steps-1, embed the latent (rounded to bf16) as the image tokens,
+ * append the embedded references and text (embedded once per call), run the denoiser
+ * for the prompt (and with guidance again for the negative prompt), and take the guided
+ * Euler step from sigmas[i] to sigmas[i + 1] (flux3_sigma_schedule).
+ * latent  device fp32 [n_img, latent_channels], updated in place (in: the initial noise,
+ *         out: the sample).  The denoiser's out_channels must equal latent_channels;
+ *         n_ref > 0 requires a 3-stream denoiser, n_ref == 0 a 2-stream one. */
+flux3_status flux3_sample_fwd(const flux3_dims *dims, const flux3_dit_weights *w, const flux3_sample_args *a,
+                              float *latent, void *ws, size_t ws_bytes, flux3_stream_t stream);
+
 /* ---- flux3_block_fwd without a caller-provided workspace.
  * This entry point has no counterpart in the model description; it is a service for
  * callers that cannot allocate device memory: for example a host program that hands all
@@ -266,7 +334,8 @@ flux3_status flux3_device_error(uint32_t *flags, int32_t reset);
 enum {
     FLUX3_KERNEL_ROPE = 1, FLUX3_KERNEL_ADALN = 2, FLUX3_KERNEL_IN_PROJ = 3,
     FLUX3_KERNEL_ATTN = 4, FLUX3_KERNEL_OUT_PROJ = 5, FLUX3_KERNEL_FINAL = 6,
-    FLUX3_KERNEL_EULER = 7, FLUX3_KERNEL_ATTN_F32 = 8
+    FLUX3_KERNEL_EULER = 7, FLUX3_KERNEL_ATTN_F32 = 8, FLUX3_KERNEL_LINEAR = 9, FLUX3_KERNEL_CFG_EULER = 10,
+    FLUX3_KERNEL_TO_BF16 = 11
 };
 flux3_status flux3_profile_begin(int32_t capacity);
 flux3_status flux3_profile_end(float *ms, int32_t *kinds, int32_t capacity, int32_t *n);
