@@ -40,7 +40,7 @@ def parse():
                    help="joint: the headline 4,256-token joint block.  The others print one line each for "
                         "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
                         "(4096+4096+160 tokens), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
-                        "loop (50 sampling steps of dit + Euler update)")
+                        "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager and as a CUDA graph)")
     return p.parse_args()
 
 
@@ -499,23 +499,19 @@ def run_workload(args):
                 return t
             fin = torch.empty(2, D, device=dev).normal_(0, 0.1, generator=g)
             return m(n_s1, 2), m(n_j, 2), fin
-        n_sets = 50 if args.workload == "loop" else 1
-        dargs = [B.DitArgs(stage1, joint, w_final, None, *mods(), 2) for _ in range(n_sets)]
+        dargs = [B.DitArgs(stage1, joint, w_final, None, *mods(), 2)]
         streams = [synth.image_stream(1024, 1024), synth.text_stream(n_txt)]
         pos = synth.positions(streams).to(dev)
         base = rnd((N, D), 1.0)
         tok = torch.empty_like(base)
         vel = torch.empty(n_img, 128, dtype=torch.float32, device=dev)
         wsp = B.workspace(B.dit_workspace_size(d, n_img, 0, n_txt), dev)
-        latent = torch.randn(n_img, 128, generator=g, device=dev)
-        sig = torch.sort(torch.rand(49, generator=torch.Generator().manual_seed(4)), descending=True).values.tolist()
-        sigmas = [1.0] + sig + [0.0]
         fwd_flops = n_s1 * (sum(block_flops(D, F, n)[0] + block_flops(D, F, n)[2] + 4.0 * n * n * D
                                 for n in (n_img, n_txt))) + n_j * sum(block_flops(D, F, N)) + 2.0 * n_img * D * 128
 
-        def forward(i=0):
+        def forward():
             tok.copy_(base)  # the stack works in place on the token buffer
-            B.dit_fwd(d, dargs[i], tok, n_img, 0, n_txt, pos, velocity=vel, ws=wsp, stream=stream)
+            B.dit_fwd(d, dargs[0], tok, n_img, 0, n_txt, pos, velocity=vel, ws=wsp, stream=stream)
 
         if args.workload == "dit":
             ms = _timed(forward, args.steps, args.warmup, stream)
@@ -525,16 +521,49 @@ def run_workload(args):
                         "config": {"tokens": N, "stage1_blocks": n_s1, "joint_blocks": n_j, "flops_per_forward": fwd_flops,
                                    "weights_gb": (n_s1 * 2 + n_j) * (3 * D + 2 * F + D + F) * D * 2 / 1e9}})
         else:
-            def loop():
-                for i in range(50):
-                    forward(i)
-                    B.euler_step(latent, vel, sigmas[i], sigmas[i + 1], stream=stream)
-            ms = _timed(loop, max(1, args.steps), 1, stream)
-            out.update({"metric": "50-step sampling loop, images/s (1024x1024)", "value": 1e3 / ms, "unit": "images/s",
-                        "ms_per_image": ms, "tflops": 50 * fwd_flops / (ms / 1e3) / 1e12, "steps": max(1, args.steps),
-                        "config": {"tokens": N, "steps_per_image": 50, "flops_per_image": 50 * fwd_flops,
-                                   "note": "token buffer reset from a fixed embedding each step (the embedders "
-                                           "are not part of this path)"}})
+            # the base-model loop through flux3_sample_fwd: 50 steps with guidance 3.5 (two
+            # denoiser calls per step), embedders 128 -> 3072 and 20,480 -> 3072, the prompt's
+            # and the negative prompt's text features embedded once per image
+            T = 20480
+            w_img, b_img = rnd((D, 128), 128 ** -0.5), None
+            w_txt, b_txt = rnd((D, T), T ** -0.5), None
+            t_pos, t_neg = rnd((n_txt, T), 1.0), rnd((n_txt, T), 1.0)
+            cfg_scale = 3.5
+            step_mods = [mods() for _ in range(50)]
+            sargs = B.SampleArgs(n_img, 0, n_txt, w_img, b_img, w_txt, b_txt, t_pos, t_neg, pos, step_mods, 50,
+                                 6.93, cfg_scale)
+            sws = B.workspace(B.sample_workspace_size(d, sargs), dev)
+            lat0 = torch.randn(n_img, 128, generator=g, device=dev)
+            lat = lat0.clone()
+
+            def image():
+                lat.copy_(lat0)
+                B.sample_fwd(d, dargs[0], sargs, lat, ws=sws, stream=stream)
+            ms = _timed(image, max(1, args.steps), 1, stream)
+            graph_ms, graph_err = None, None
+            try:
+                # the whole 50-step call captured once and replayed (the library allocates
+                # nothing and launches only on the caller's stream)
+                gr = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    image()
+                stream.wait_stream(side)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(gr, stream=side):
+                    lat.copy_(lat0)
+                    B.sample_fwd(d, dargs[0], sargs, lat, ws=sws, stream=side)
+                graph_ms = _timed(gr.replay, max(1, args.steps), 1, stream)
+            except Exception as e:  # report, do not hide, a capture failure
+                graph_err = f"{type(e).__name__}: {e}"
+            img_flops = 50 * 2 * fwd_flops
+            out.update({"metric": "50-step guided sampling loop, images/s (1024x1024)", "value": 1e3 / ms,
+                        "unit": "images/s", "ms_per_image": ms, "tflops": img_flops / (ms / 1e3) / 1e12,
+                        "graph_ms_per_image": graph_ms, "graph_error": graph_err, "steps": max(1, args.steps),
+                        "config": {"tokens": N, "steps_per_image": 50, "cfg_scale": cfg_scale,
+                                   "denoiser_calls_per_image": 100, "flops_per_image": img_flops,
+                                   "alpha": 6.93}})
     assert B.device_error() == 0
     print(json.dumps(out), flush=True)
 

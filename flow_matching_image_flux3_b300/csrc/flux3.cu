@@ -58,6 +58,21 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute persists;
+// setting it again on every launch is host work, and is not a stream operation a graph
+// capture can record).
+// (one flag array per kernel: the kernel is the template argument)
+template <auto Kernel>
+bool smem_attr_once(int bytes) {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done[dev] = true;
+    return true;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -210,8 +225,7 @@ flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
     const int tasks = (P.m_tiles / CL) * P.n_tiles;
     if (tasks == 0) return FLUX3_OK;
     const int smem = GemmCfg<BN>::SMEM_BYTES;
-    if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, EPI, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return FLUX3_ERR_CUDA;
+    if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL>>(smem)) return FLUX3_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return FLUX3_ERR_CUDA;
     if constexpr (CL == 1) {
@@ -345,8 +359,7 @@ flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const v
     P.ld_out = ld_out;
     P.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
     if (pairs == 0) return FLUX3_OK;
-    if (cudaFuncSetAttribute(attn_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_BYTES) != cudaSuccess)
-        return FLUX3_ERR_CUDA;
+    if (!smem_attr_once<attn_tcgen05_kernel>(ATT_SMEM_BYTES)) return FLUX3_ERR_CUDA;
     prof_before(FLUX3_KERNEL_ATTN, st);
     attn_tcgen05_kernel<<<dim3(pairs, H), ATT_THREADS, ATT_SMEM_BYTES, st>>>(P);
     prof_after(st);
