@@ -36,10 +36,12 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=["joint", "stage1", "joint_ref", "dit", "loop"], default="joint",
+    p.add_argument("--workload", choices=["joint", "stage1", "joint_ref", "refs10", "refs10_s1", "dit", "loop"],
+                   default="joint",
                    help="joint: the headline 4,256-token joint block.  The others print one line each for "
                         "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
-                        "(4096+4096+160 tokens), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
+                        "(4096+4096+160 tokens), refs10 / refs10_s1 (image + ten references + text = 45,216 "
+                        "tokens, joint / per-stream block), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
                         "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager and as a CUDA graph)")
     return p.parse_args()
 
@@ -430,8 +432,11 @@ def run_workload(args):
     stream = torch.cuda.current_stream()
     out = {"impl": "ours", "workload": args.workload, "n_gpus": 1, "data": "synthetic", "dtype": "bf16",
            "higher_is_better": True, "unit": "tokens/s"}
-    if args.workload in ("stage1", "joint_ref"):
-        case = synth.config(2 if args.workload == "stage1" else 3)
+    if args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1"):
+        if args.workload.startswith("refs10"):
+            case = synth.config_refs(10, 1 if args.workload == "refs10_s1" else 2, seed=5)
+        else:
+            case = synth.config(2 if args.workload == "stage1" else 3)
         d, N = case.dims, case.n
         D, F = d.width, d.ffn_hidden
 

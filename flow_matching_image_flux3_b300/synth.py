@@ -177,6 +177,24 @@ def config(idx: int, bias: bool = False) -> BlockCase:
     raise ValueError(idx)
 
 
+def config_refs(n_refs: int, stage: int, seed: int, bias: bool = False) -> BlockCase:
+    """Multi-reference editing at 1024^2: the image, n_refs references of 4,096 tokens each
+    (reference k at t = k + 1 on the image's (h, w) grid) and 160 text tokens.  The
+    references form one stream: one segment for modulation and, in stage 1, one
+    self-attending range and weight set."""
+    img = image_stream(1024, 1024)
+    refs = [image_stream(1024, 1024, t=k + 1, kind="ref") for k in range(n_refs)]
+    txt = text_stream(160)
+    g = torch.Generator("cpu").manual_seed(seed)
+    dims = FULL
+    n = img.n + sum(r.n for r in refs) + txt.n
+    x = _randn(g, (n, dims.width)).to(torch.bfloat16)
+    weights = [draw_weights(g, dims, bias) for _ in range(1 if stage == 2 else 3)]
+    mod = draw_mod(g, 3, dims.width)
+    seg_off = [0, img.n, img.n + sum(r.n for r in refs), n]
+    return BlockCase(dims, x, positions([img] + refs + [txt]), seg_off, mod, weights, stage, [img] + refs + [txt])
+
+
 def as_f64(t: torch.Tensor) -> np.ndarray:
     """Exact upcast of a CPU tensor (bf16 or fp32) to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()

@@ -6,6 +6,6 @@ and shares no code with it.
 """
 from .flux3_block import (  # noqa: F401
     round_bf16, layer_norm, segment_ids, modulate, ada_ln, rope_angles, rope_rotate,
-    rms_norm, attention, swiglu, Weights, BlockOut, block_forward, final_layer,
+    rms_norm, attention, attention_rows, swiglu, Weights, BlockOut, block_forward, final_layer,
     dit_forward, euler_step, block_forward_rows, block_keys_values,
 )

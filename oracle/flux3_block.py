@@ -159,6 +159,33 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
     return out.reshape(n, h * d)
 
 
+def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: Sequence[int],
+                   groups: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+    """Rows `rows` of attention(q, k, v, groups), for sequences too long for the full
+    score matrix: each sampled query row attends to the keys of its own range, one head
+    at a time.  q, k, v [N, H, d] (any float dtype; computed in float64) -> [len(rows), H*d]."""
+    n, h, d = k.shape
+    if groups is None:
+        groups = [(0, n)]
+    rows = list(rows)
+    own = []
+    for r in rows:
+        rng = [(a, b) for a, b in groups if a <= r < b]
+        assert len(rng) == 1, "every sampled row must fall in exactly one range"
+        own.append(rng[0])
+    out = np.zeros((len(rows), h, d), dtype=F64)
+    scale = 1.0 / math.sqrt(d)
+    for hh in range(h):
+        kh = np.asarray(k[:, hh], dtype=F64)
+        vh = np.asarray(v[:, hh], dtype=F64)
+        for i, r in enumerate(rows):
+            a, b = own[i]
+            s = kh[a:b] @ np.asarray(q[r, hh], dtype=F64) * scale
+            p = np.exp(s - s.max())
+            out[i, hh] = (p / p.sum()) @ vh[a:b]
+    return out.reshape(len(rows), h * d)
+
+
 def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     """silu(g) * u with silu(g) = g / (1 + exp(-g))."""
     return g / (1.0 + np.exp(-g)) * u

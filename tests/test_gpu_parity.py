@@ -145,6 +145,26 @@ def test_attention_peaked_scores_and_out_stride():
     assert torch.all(out[:, 256:] == 7.0)
 
 
+@pytest.mark.parametrize("stage", [2, 1])
+def test_attention_ten_references_sampled(stage):
+    # multi-reference editing: a 1024^2 image, ten 1024^2 references (one stream) and 160
+    # text tokens = 45,216 tokens; the whole sequence runs on the device, sampled query rows
+    # (tile and stream boundaries, the last row, random rows) are checked against all keys
+    H, N = 24, 4096 + 40960 + 160
+    seg = [0, 4096, 45056, N]
+    g = torch.Generator(device="cuda").manual_seed(100 + stage)
+    q, k, v = (torch.randn(H, N, 128, generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    vt = torch.zeros(H, 128, B.ld_vt(N), dtype=torch.bfloat16, device="cuda")
+    vt[:, :, :N] = v.transpose(1, 2)
+    out = B.attn_fwd(synth.FULL, q, k, vt, None if stage == 2 else seg)
+    rows = sorted({0, 1, 127, 128, 255, 256, 4095, 4096, 4097, 20000, 44999, 45055, 45056, 45100, N - 1} |
+                  set(np.random.default_rng(stage).choice(N, 8, replace=False).tolist()))
+    groups = None if stage == 2 else [(seg[i], seg[i + 1]) for i in range(3)]
+    cpu = [t.float().cpu().transpose(0, 1).numpy() for t in (q, k, v)]   # [N, H, 128], exact bf16 values
+    ref = O.attention_rows(cpu[0], cpu[1], cpu[2], rows, groups)
+    assert_close("attn (10 references)", f64(out[rows]), ref)
+
+
 # ------------------------------------------------------------------ a9 output projection
 @pytest.mark.parametrize("n,seg,stage", [(144, [0, 64, 144], 2), (1, [0, 1], 2), (290, [0, 130, 290], 2),
                                          (200, [0, 50, 120, 200], 1)])

@@ -402,3 +402,13 @@ def test_block_keys_values_of_some_rows_match_all_rows():
     np.testing.assert_allclose(v2, v[rows], rtol=1e-13, atol=1e-13)
     full = _run(case)
     np.testing.assert_allclose(k, full.k, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_rows_match_full_attention():
+    # the sampled-rows form of attention against the full (pinned) one, joint and per range
+    q, k, v = (rng.standard_normal((150, 3, 128)) for _ in range(3))
+    rows = [0, 1, 63, 64, 100, 149]
+    np.testing.assert_allclose(O.attention_rows(q, k, v, rows), O.attention(q, k, v)[rows], rtol=1e-12, atol=1e-12)
+    groups = [(0, 64), (64, 140), (140, 150)]
+    np.testing.assert_allclose(O.attention_rows(q, k, v, rows, groups), O.attention(q, k, v, groups)[rows],
+                               rtol=1e-12, atol=1e-12)
