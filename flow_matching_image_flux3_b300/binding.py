@@ -20,7 +20,7 @@ c_i32, c_f32, c_vp, c_size = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ct
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 MAX_SEGMENTS = 16
 KERNEL_NAMES = {1: "rope", 2: "adaln", 3: "in_proj", 4: "attn", 5: "out_proj", 6: "final", 7: "euler", 8: "attn_f32",
-                9: "linear", 10: "cfg_euler", 11: "to_bf16"}
+                9: "linear", 10: "cfg_euler", 11: "to_bf16", 12: "quantize"}
 
 
 class flux3_dims(ctypes.Structure):
@@ -30,6 +30,11 @@ class flux3_dims(ctypes.Structure):
 
 class flux3_block_weights(ctypes.Structure):
     _fields_ = [("w_in", c_vp), ("b_in", c_vp), ("q_norm", c_vp), ("k_norm", c_vp), ("w_out", c_vp), ("b_out", c_vp)]
+
+
+class flux3_block_weights_fp8(ctypes.Structure):
+    _fields_ = [("w_in", c_vp), ("s_in", c_vp), ("b_in", c_vp), ("q_norm", c_vp), ("k_norm", c_vp), ("w_out", c_vp),
+                ("b_out", c_vp)]
 
 
 class flux3_segments(ctypes.Structure):
@@ -90,6 +95,12 @@ def _load() -> ctypes.CDLL:
         "flux3_linear_fwd": (c_i32, [P(flux3_dims), c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp]),
         "flux3_cfg_euler_step": (c_i32, [c_vp, c_vp, c_vp, ctypes.c_int64, c_f32, c_f32, c_f32, c_vp, c_vp]),
         "flux3_sample_workspace_size": (c_size, [P(flux3_dims), P(flux3_sample_args)]),
+        "flux3_quantize_rows_fp8": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),
+        "flux3_in_proj_fp8_fwd": (c_i32, [P(flux3_dims), P(flux3_block_weights_fp8), c_i32, P(flux3_segments), c_vp,
+                                          c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp]),
+        "flux3_block_fp8_workspace_size": (c_size, [P(flux3_dims), c_i32]),
+        "flux3_block_fp8_fwd": (c_i32, [P(flux3_dims), P(flux3_block_weights_fp8), P(flux3_segments), c_vp, c_vp,
+                                        c_i32, c_vp, c_vp, c_size, c_vp]),
         "flux3_sample_fwd": (c_i32, [P(flux3_dims), P(flux3_dit_weights), P(flux3_sample_args), c_vp, c_vp, c_size,
                                      c_vp]),
         "flux3_block_fwd_static": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp,
@@ -112,7 +123,8 @@ EXPORTED = [
     "flux3_stream_block_fwd", "flux3_final_fwd", "flux3_dit_workspace_size", "flux3_dit_fwd", "flux3_euler_step",
     "flux3_device_error", "flux3_profile_begin", "flux3_profile_end", "flux3_block_fwd_static",
     "flux3_sigma_schedule", "flux3_linear_fwd", "flux3_cfg_euler_step", "flux3_sample_workspace_size",
-    "flux3_sample_fwd",
+    "flux3_sample_fwd", "flux3_quantize_rows_fp8", "flux3_in_proj_fp8_fwd", "flux3_block_fp8_workspace_size",
+    "flux3_block_fp8_fwd",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -413,6 +425,72 @@ def sample_fwd(dims, dit: "DitArgs", args: SampleArgs, latent: torch.Tensor, ws:
                                                     _ptr(latent, torch.float32), _ptr(ws), ws.numel(),
                                                     _stream(stream)))
     return latent
+
+
+def quantize_rows_fp8(x: torch.Tensor, stream=None):
+    """Row-wise e4m3 codes (uint8 [rows, k]) and fp32 scales [rows] of a bf16 matrix."""
+    rows, k = x.shape
+    q = torch.empty(rows, k, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check("flux3_quantize_rows_fp8", lib.flux3_quantize_rows_fp8(_ptr(x, torch.bfloat16), rows, k, _ptr(q), _ptr(sc),
+                                                                  _stream(stream)))
+    return q, sc
+
+
+class Fp8Weights:
+    """A block's weights with the input projection quantized row-wise to e4m3 (on the
+    device, through flux3_quantize_rows_fp8); W_out, norms and biases as given."""
+
+    def __init__(self, w, stream=None):
+        self.w_in, self.s_in = quantize_rows_fp8(w.w_in, stream)
+        self.b_in, self.q_norm, self.k_norm = w.b_in, w.q_norm, w.k_norm
+        self.w_out, self.b_out = w.w_out, w.b_out
+
+
+def _fp8_struct(w: Fp8Weights) -> flux3_block_weights_fp8:
+    return flux3_block_weights_fp8(_ptr(w.w_in, torch.uint8), _ptr(w.s_in, torch.float32), _ptr(w.b_in, torch.float32),
+                                   _ptr(w.q_norm, torch.float32), _ptr(w.k_norm, torch.float32),
+                                   _ptr(w.w_out, torch.bfloat16), _ptr(w.b_out, torch.float32))
+
+
+def in_proj_fp8_fwd(dims, weights: Sequence[Fp8Weights], seg_off: Sequence[int], a8: torch.Tensor, sa: torch.Tensor,
+                    rope: torch.Tensor, stream=None):
+    """in_proj_fwd on e4m3 codes a8 (uint8 [N, D]) with per-token scales sa (fp32 [N])."""
+    n = a8.shape[0]
+    D, H, F = dims.width, dims.heads, dims.ffn_hidden
+    dev = a8.device
+    q = torch.empty(H, n, 128, dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    ldv = ld_vt(n)
+    vt = torch.zeros(H, 128, ldv, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(n, D + F, dtype=torch.bfloat16, device=dev)
+    d, s = make_dims(dims), Segments(seg_off, None)
+    wa = (flux3_block_weights_fp8 * len(weights))(*[_fp8_struct(w) for w in weights])
+    _check("flux3_in_proj_fp8_fwd", lib.flux3_in_proj_fp8_fwd(
+        ctypes.byref(d), wa, len(weights), ctypes.byref(s.s), _ptr(a8, torch.uint8), _ptr(sa, torch.float32), n,
+        _ptr(rope, torch.float32), _ptr(q), _ptr(k), _ptr(vt), ldv, _ptr(y), _stream(stream)))
+    return q, k, vt, y
+
+
+def block_fp8_workspace_size(dims, n: int) -> int:
+    d = make_dims(dims)
+    return int(lib.flux3_block_fp8_workspace_size(ctypes.byref(d), n))
+
+
+def block_fp8_fwd(dims, weights: Fp8Weights, seg_off: Sequence[int], mod: torch.Tensor, x: torch.Tensor,
+                  rope: torch.Tensor, x_out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """The joint block with the e4m3 input projection."""
+    n = x.shape[0]
+    x_out = x_out if x_out is not None else torch.empty_like(x)
+    ws = ws if ws is not None else workspace(block_fp8_workspace_size(dims, n), x.device)
+    d, s = make_dims(dims), Segments(seg_off, mod)
+    w = _fp8_struct(weights)
+    _check("flux3_block_fp8_fwd", lib.flux3_block_fp8_fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(s.s),
+                                                          _ptr(x, torch.bfloat16), _ptr(x_out, torch.bfloat16), n,
+                                                          _ptr(rope, torch.float32), _ptr(ws), ws.numel(),
+                                                          _stream(stream)))
+    return x_out
 
 
 def device_error(reset: bool = True) -> int:

@@ -47,6 +47,16 @@ bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// 8-bit codes (e4m3) row-major [outer, inner], box 128 x box_outer (128 bytes), 128-byte swizzle
+bool tmap_2d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 // bf16 [d2][d1][d0], strides in bytes, box 64 x 128 x 1, 128-byte swizzle
 bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2) {
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -197,7 +207,7 @@ flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& 
 
 // Clusters of two CTAs that can be resident at once for a GEMM instantiation (SMs are
 // paired within a GPC, so this can be below half the SM count); cached per device.
-template <int BN, int EPI>
+template <int BN, int EPI, int AK>
 int max_active_pairs(int smem, int sms) {
     static int cache[64] = {};
     int dev = 0;
@@ -215,27 +225,27 @@ int max_active_pairs(int smem, int sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<BN, EPI, 2>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<BN, EPI, 2, AK>, &cfg) != cudaSuccess) return 0;
     cache[dev] = n;
     return n;
 }
 
-template <int BN, int EPI, int CL>
+template <int BN, int EPI, int CL, int AK = 0>
 flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
     const int tasks = (P.m_tiles / CL) * P.n_tiles;
     if (tasks == 0) return FLUX3_OK;
     const int smem = GemmCfg<BN>::SMEM_BYTES;
-    if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL>>(smem)) return FLUX3_ERR_CUDA;
+    if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL, AK>>(smem)) return FLUX3_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return FLUX3_ERR_CUDA;
     if constexpr (CL == 1) {
         const int grid = tasks < sms ? tasks : sms;
         prof_before(kind, st);
-        gemm_tcgen05_kernel<BN, EPI, CL><<<grid, GEMM_THREADS, smem, st>>>(P);
+        gemm_tcgen05_kernel<BN, EPI, CL, AK><<<grid, GEMM_THREADS, smem, st>>>(P);
         prof_after(st);
         return launch_status();
     } else {
-    const int pairs = max_active_pairs<BN, EPI>(smem, sms);
+    const int pairs = max_active_pairs<BN, EPI, AK>(smem, sms);
     if (pairs <= 0) return FLUX3_ERR_CUDA;
     const int units = tasks < pairs ? tasks : pairs;  // persistent: every cluster resident at once
     cudaLaunchConfig_t cfg = {};
@@ -251,7 +261,7 @@ flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     prof_before(kind, st);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, EPI, CL>, P);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, EPI, CL, AK>, P);
     prof_after(st);
     return e == cudaSuccess ? launch_status() : FLUX3_ERR_CUDA;
     }
@@ -297,6 +307,42 @@ flux3_status run_in_proj(const flux3_dims* d, const flux3_block_weights* w, int 
     P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
     P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
     return launch_gemm<256, EPI_QKV_SWIGLU, 2>(P, st, FLUX3_KERNEL_IN_PROJ);
+}
+
+// the input projection on e4m3 operands: a8 [N, D] codes with per-token scales sa, each
+// weight set's e4m3 W_in with per-row scales
+flux3_status run_in_proj_fp8(const flux3_dims* d, const flux3_block_weights_fp8* w, int n_w, const flux3_segments* segs,
+                             const void* a8, const float* sa, int N, const float* rope, void* q, void* k, void* vt,
+                             int ld_vt, void* y, cudaStream_t st) {
+    if (N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    const int D = d->width, F = d->ffn_hidden, H = d->heads;
+    const int n_in = 3 * D + 2 * F;
+    if (!tmap_2d_u8(&P.tm_a, a8, D, N, (uint64_t)D, 128)) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < n_w; ++i) {
+        if (!tmap_2d_u8(&P.tm_b[i], w[i].w_in, D, n_in, (uint64_t)D, 128)) return FLUX3_ERR_INVALID_ARG;
+        P.ew[i] = {w[i].b_in, w[i].q_norm, w[i].k_norm, w[i].s_in};
+    }
+    fill_groups(P, segs->seg_off, segs->n_seg, n_w, N, 2);
+    P.n_tiles = 3 * H / 2 + F / 128;
+    P.k_blocks = D / 128;
+    P.a_scale = sa;
+    P.heads = H; P.width = D; P.ffn = F; P.n_tokens = N; P.ld_vt = ld_vt; P.ld_y = D + F;
+    P.rms_eps = d->rms_eps;
+    P.rope = rope;
+    P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
+    P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
+    return launch_gemm<256, EPI_QKV_SWIGLU, 2, 1>(P, st, FLUX3_KERNEL_IN_PROJ);
+}
+
+flux3_status run_quantize_rows(const void* x, int rows, int k, void* q, float* scale, cudaStream_t st) {
+    if (rows == 0) return FLUX3_OK;
+    prof_before(FLUX3_KERNEL_QUANTIZE, st);
+    quantize_rows_e4m3_kernel<<<(rows + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, k,
+                                                             static_cast<uint8_t*>(q), scale);
+    prof_after(st);
+    return launch_status();
 }
 
 flux3_status run_out_proj(const flux3_dims* d, const flux3_block_weights* w, int n_w, const flux3_segments* segs, const void* y,
@@ -832,6 +878,78 @@ flux3_status flux3_sample_fwd(const flux3_dims* dims, const flux3_dit_weights* w
             return s;
     }
     return FLUX3_OK;
+}
+
+flux3_status flux3_quantize_rows_fp8(const void* x, int32_t rows, int32_t k, void* q, float* scale, flux3_stream_t stream) {
+    if (rows < 0 || rows > kMaxTokens * 16 || k <= 0 || k > (1 << 20)) return FLUX3_ERR_INVALID_ARG;
+    if (k % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (rows == 0) return FLUX3_OK;
+    if (!x || !q || !scale || !al16(x) || !al16(q)) return FLUX3_ERR_INVALID_ARG;
+    return run_quantize_rows(x, rows, k, q, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static flux3_status check_weights_fp8(const flux3_block_weights_fp8* w, int n_w) {
+    if (!w || n_w < 1 || n_w > FLUX3_MAX_SEGMENTS) return FLUX3_ERR_INVALID_ARG;
+    for (int i = 0; i < n_w; ++i)
+        if (!w[i].w_in || !al16(w[i].w_in) || !w[i].s_in || !al16(w[i].s_in) || !w[i].q_norm || !al16(w[i].q_norm) ||
+            !w[i].k_norm || !al16(w[i].k_norm) || (w[i].b_in && !al16(w[i].b_in)))
+            return FLUX3_ERR_INVALID_ARG;
+    return FLUX3_OK;
+}
+
+flux3_status flux3_in_proj_fp8_fwd(const flux3_dims* dims, const flux3_block_weights_fp8* w, int32_t n_w,
+                                   const flux3_segments* segs, const void* a8, const float* sa, int32_t n_tokens,
+                                   const float* rope, void* q, void* k, void* vt, int32_t ld_vt, void* y,
+                                   flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (dims->width % 128 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, n_tokens, false)) != FLUX3_OK) return s;
+    if ((s = check_weights_fp8(w, n_w)) != FLUX3_OK) return s;
+    if (n_w != 1 && n_w != segs->n_seg) return FLUX3_ERR_INVALID_ARG;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!a8 || !sa || !rope || !q || !k || !vt || !y) return FLUX3_ERR_INVALID_ARG;
+    if (!al16(a8) || !al16(rope) || !al16(q) || !al16(k) || !al16(vt) || !al16(y)) return FLUX3_ERR_INVALID_ARG;
+    if (ld_vt < n_tokens || ld_vt % 8 != 0) return FLUX3_ERR_INVALID_ARG;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    return run_in_proj_fp8(dims, w, n_w, segs, a8, sa, n_tokens, rope, q, k, vt, ld_vt, y,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t flux3_block_fp8_workspace_size(const flux3_dims* dims, int32_t n_tokens) {
+    if (check_dims(dims) != FLUX3_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
+    return block_ws_layout(dims, n_tokens, nullptr).bytes + up256((size_t)n_tokens * dims->width) +
+           up256((size_t)n_tokens * 4);
+}
+
+flux3_status flux3_block_fp8_fwd(const flux3_dims* dims, const flux3_block_weights_fp8* w, const flux3_segments* segs,
+                                 const void* x, void* x_out, int32_t n_tokens, const float* rope, void* ws, size_t ws_bytes,
+                                 flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (dims->width % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    const int N = n_tokens;
+    if (N < 0 || N > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, N, true)) != FLUX3_OK) return s;
+    if ((s = check_weights_fp8(w, 1)) != FLUX3_OK) return s;
+    if (!w->w_out || !al16(w->w_out) || (w->b_out && !al16(w->b_out))) return FLUX3_ERR_INVALID_ARG;
+    if (N == 0) return FLUX3_OK;
+    if (!x || !x_out || !rope || !al16(x) || !al16(x_out) || !al16(rope)) return FLUX3_ERR_INVALID_ARG;
+    if (!ws || !al256(ws) || ws_bytes < flux3_block_fp8_workspace_size(dims, N)) return FLUX3_ERR_WORKSPACE;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const BlockWs b = block_ws_layout(dims, N, static_cast<uint8_t*>(ws));
+    uint8_t* a8 = static_cast<uint8_t*>(ws) + b.bytes;
+    float* sa = reinterpret_cast<float*>(a8 + up256((size_t)N * dims->width));
+    const int D = dims->width, F = dims->ffn_hidden;
+    if ((s = run_adaln(dims, segs->mod, seg_table(segs->seg_off, segs->n_seg), x, N, b.a, st)) != FLUX3_OK) return s;
+    if ((s = run_quantize_rows(b.a, N, D, a8, sa, st)) != FLUX3_OK) return s;
+    if ((s = run_in_proj_fp8(dims, w, 1, segs, a8, sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK) return s;
+    const int32_t full[2] = {0, N};
+    if ((s = run_attn(dims, b.q, b.k, b.vt, b.ld_vt, N, full, 1, b.y, D + F, false, st)) != FLUX3_OK) return s;
+    const flux3_block_weights wo{nullptr, nullptr, nullptr, nullptr, w->w_out, w->b_out};
+    return run_out_proj(dims, &wo, 1, segs, b.y, x, x_out, N, st);
 }
 
 flux3_status flux3_device_error(uint32_t* flags, int32_t reset) {

@@ -31,6 +31,7 @@ struct EpiWeights {
     const float* bias;
     const float* q_norm;
     const float* k_norm;
+    const float* w_scale;  // e4m3 operands: scale of each weight row (output column)
 };
 
 struct GemmParams {
@@ -40,6 +41,7 @@ struct GemmParams {
     GemmGroup grp[FLUX3_MAX_SEGMENTS];
     int n_groups;
     int m_tiles, n_tiles, k_blocks;
+    const float* a_scale;  // e4m3 operands: scale of each A row (token)
     // EPI_QKV_SWIGLU
     int heads, width, ffn, n_tokens, ld_vt, ld_y;
     float rms_eps;
@@ -103,8 +105,12 @@ F3_DEV void unpack32(const uint32_t (&r)[32], float* v) {
 }
 
 // --------------------------------------------------------------------- epilogues
+// AK = 1: the operands were e4m3 codes; the accumulator is scaled by the token's and the
+// weight row's scales before the epilogue proper.
+template <int AK>
 F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
     const int nq = 3 * p.heads / 2;
+    const float sa = AK ? p.a_scale[r] : 1.f;
     if (n < nq) {
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
@@ -120,6 +126,14 @@ F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
                 unpack32(t, v + c * 32);
             }
             if (!valid) continue;
+            if (AK) {
+                const float4* s4 = reinterpret_cast<const float4*>(w.w_scale + hg * 128);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float4 sw = __ldg(s4 + i);
+                    v[4 * i] *= sa * sw.x; v[4 * i + 1] *= sa * sw.y; v[4 * i + 2] *= sa * sw.z; v[4 * i + 3] *= sa * sw.w;
+                }
+            }
             if (w.bias) {
                 const float4* b4 = reinterpret_cast<const float4*>(w.bias + hg * 128);
 #pragma unroll
@@ -175,6 +189,12 @@ F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
             float g[32], u[32];
             unpack32(tg, g);
             unpack32(tu, u);
+            if (AK) {
+                const float* sg = w.w_scale + 3 * p.width + 128 * j + c * 32;
+                const float* su = sg + p.ffn;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) { g[i] *= sa * __ldg(sg + i); u[i] *= sa * __ldg(su + i); }
+            }
             if (bg) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) { g[i] += __ldg(bg + c * 32 + i); u[i] += __ldg(bu + c * 32 + i); }
@@ -316,9 +336,12 @@ F3_DEV TileInfo tile_info(const GemmParams& p, int task, int rank, int cl) {
     return {n, g, p.grp[g].row_begin + (mt - p.grp[g].tile_begin) * GEMM_BM, kb0};
 }
 
-template <int BN, int EPI, int CL>
+// AK: operand kind, 0 = bf16 (64 elements per 128-byte row of a k-block), 1 = e4m3 (128).
+template <int BN, int EPI, int CL, int AK = 0>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
     static_assert(CL == 1 || (CL == 2 && BN == 256), "clusters of two split a 256-row B tile");
+    static_assert(AK == 0 || EPI == EPI_QKV_SWIGLU, "e4m3 operands: input projection only");
+    constexpr int KB_ELEMS = AK ? 128 : GEMM_BK;
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -384,7 +407,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
                     const uint32_t sb = sa + C::A_BYTES;
                     int kr = ti.kb0 + kb;
                     if (kr >= p.k_blocks) kr -= p.k_blocks;
-                    const int kc = kr * GEMM_BK;
+                    const int kc = kr * KB_ELEMS;
                     mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
                     tma_load_2d(sa, &p.tm_a, full_bar(s), kc, ti.row0);
                     if (CL == 2) {
@@ -413,7 +436,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
     } else if (warp == 1) {
         // ---------------- MMA issuer (converged warp, one elected lane issues)
         const bool leader = elect_one();
-        constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN);
+        constexpr uint32_t IDESC = AK ? idesc_e4m3_f32(GEMM_BM, BN) : idesc_bf16_f32(GEMM_BM, BN);
         int s = 0;
         uint32_t ph = 0;
         int acc = 0;
@@ -430,8 +453,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
                 const uint64_t ad = sdesc_kmajor_sw128(sa);
                 const uint64_t bd = sdesc_kmajor_sw128(sa + C::A_BYTES);
 #pragma unroll
-                for (int k = 0; k < GEMM_BK / 16; ++k)
-                    mma_bf16_ss_if(leader, d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
+                for (int k = 0; k < 4; ++k) {  // 32 bytes of each row per instruction
+                    if (AK) mma_e4m3_ss_if(leader, d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
+                    else mma_bf16_ss_if(leader, d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, (kb | k) != 0);
+                }
                 if (CL == 2) mma_commit_multicast_if(leader, empty_bar(s), kPair);
                 else mma_commit_if(leader, empty_bar(s));
                 if (++s == C::STAGES) { s = 0; ph ^= 1u; }
@@ -460,7 +485,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16) + acc * BN;
             const EpiWeights& w = p.ew[p.grp[ti.g].wset];
-            if (EPI == EPI_QKV_SWIGLU) epi_qkv(p, w, ti.n, tacc, valid ? r : 0, valid);
+            if (EPI == EPI_QKV_SWIGLU) epi_qkv<AK>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_F32) epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);

@@ -208,6 +208,47 @@ inline bool launch_adaln(int D, const __nv_bfloat16* x, int n_rows, float eps, c
     }
 }
 
+// ---------------------------------------------------------------- e4m3 row quantization
+// One warp per row of a bf16 [rows, k] matrix (k % 256 == 0): amax of the row (exact on
+// bf16 values), scale = amax / 448 and inv = 448 / amax in fp32 (IEEE division), codes =
+// e4m3(x * inv) rounded to nearest even and saturated at +-448 (cvt.rn.satfinite).  An
+// all-zero row gets zero codes and scale 0.
+__global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ x, int rows, int k,
+                                                                uint8_t* __restrict__ q, float* __restrict__ scale) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= rows) return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * k);
+    const int chunks = k / 256;
+    float amax = 0.f;
+    for (int c = 0; c < chunks; ++c) {
+        const uint4 u = __ldg(xr + c * 32 + lane);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+    if (lane == 0) scale[r] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
+    uint2* qr = reinterpret_cast<uint2*>(q + (size_t)r * k);
+    for (int c = 0; c < chunks; ++c) {
+        const uint4 u = __ldg(xr + c * 32 + lane);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = __fmul_rn(__uint_as_float(w[e] << 16), inv);
+            const float hi = __fmul_rn(__uint_as_float(w[e] & 0xffff0000u), inv);
+            uint16_t h;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));  // low byte = lo
+            pk[e] = h;
+        }
+        qr[c * 32 + lane] = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+    }
+}
+
 // ---------------------------------------------------------------- guided Euler update
 // latent += dt * (v_neg + s (v_pos - v_neg)) (v_neg == nullptr: latent += dt * v_pos); the
 // updated latent rounded to bf16 goes to lat_bf (the next step's embedder input) if given.

@@ -211,6 +211,17 @@ F3_DEV void mma_bf16_ts_if(bool issue, uint32_t d_tmem, uint32_t a_tmem, uint64_
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"((uint32_t)issue)
         : "memory");
 }
+// The same for e4m3 x e4m3 operands (kind::f8f6f4: K = 32 per instruction, 32 bytes of
+// each row, the same byte layout as bf16's K = 16).
+F3_DEV void mma_e4m3_ss_if(bool issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"((uint32_t)issue)
+        : "memory");
+}
 F3_DEV void mma_commit_if(bool issue, uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred q;\n\t"
@@ -287,6 +298,12 @@ F3_DEV uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 // Instruction descriptor, kind::f16: A = B = bf16, D = fp32, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: A = B = e4m3 (format code 0), D = fp32, both
+// K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ small helpers

@@ -297,6 +297,53 @@ size_t flux3_sample_workspace_size(const flux3_dims *dims, const flux3_sample_ar
 flux3_status flux3_sample_fwd(const flux3_dims *dims, const flux3_dit_weights *w, const flux3_sample_args *a,
                               float *latent, void *ws, size_t ws_bytes, flux3_stream_t stream);
 
+/* ---- FP8 (e4m3) row-wise input projection.  The pages run quantized variants of the DiT's
+ * projections (SGLang cookbook FLUX.3, section 7: FP8 and NVFP4 checkpoints; the Miles
+ * page, section 3: "fp8 rowwise").  Here the input projection multiplies e4m3 codes on
+ * the tensor cores (kind::f8f6f4) with fp32 accumulation:
+ *   P = s_a[token] * (a_q W_q^T)[token, out] * s_w[out] + b_in
+ * then the same epilogues as flux3_in_proj_fwd.  The output projection stays bf16.
+ * Quantization (flux3_quantize_rows_fp8) is per row: scale = amax / 448, codes =
+ * e4m3(x * (448 / amax)) rounded to nearest even, saturated at +-448, all in fp32
+ * (an all-zero row: zero codes, scale 0).  NVFP4 (block-scaled) is not provided. */
+
+/* Row-wise e4m3 quantization of a bf16 [rows, k] matrix, k % 256 == 0.
+ * q      device uint8 [rows, k]: e4m3 codes;  scale  device fp32 [rows]. */
+flux3_status flux3_quantize_rows_fp8(const void *x, int32_t rows, int32_t k, void *q, float *scale,
+                                     flux3_stream_t stream);
+
+/* One block's parameters with an e4m3 input projection (device memory).
+ *  w_in   uint8 [3D + 2F, D]: e4m3 codes of W_in (rows Q | K | V | gate | up), quantized
+ *         per row (flux3_quantize_rows_fp8);  s_in  fp32 [3D + 2F]: their scales.
+ *  Other fields as flux3_block_weights. */
+typedef struct flux3_block_weights_fp8 {
+    const void *w_in;
+    const float *s_in;
+    const float *b_in;
+    const float *q_norm;
+    const float *k_norm;
+    const void *w_out;
+    const float *b_out;
+} flux3_block_weights_fp8;
+
+/* flux3_in_proj_fwd on e4m3 operands: a8  device uint8 [N, D] codes of the modulated input,
+ * sa  device fp32 [N] their per-token scales; w, n_w as flux3_in_proj_fwd (fp8 weight sets).
+ * D % 128 == 0.  Outputs and other arguments as flux3_in_proj_fwd. */
+flux3_status flux3_in_proj_fp8_fwd(const flux3_dims *dims, const flux3_block_weights_fp8 *w, int32_t n_w,
+                                   const flux3_segments *segs, const void *a8, const float *sa, int32_t n_tokens,
+                                   const float *rope, void *q, void *k, void *vt, int32_t ld_vt, void *y,
+                                   flux3_stream_t stream);
+
+size_t flux3_block_fp8_workspace_size(const flux3_dims *dims, int32_t n_tokens);
+
+/* The joint block (stage 2) with the e4m3 input projection: LayerNorm + modulation (bf16),
+ * row quantization, FP8 input projection with its epilogues, attention, bf16 output
+ * projection with the gated residual.  Arguments as flux3_block_fwd; workspace
+ * flux3_block_fp8_workspace_size bytes. */
+flux3_status flux3_block_fp8_fwd(const flux3_dims *dims, const flux3_block_weights_fp8 *w, const flux3_segments *segs,
+                                 const void *x, void *x_out, int32_t n_tokens, const float *rope, void *ws,
+                                 size_t ws_bytes, flux3_stream_t stream);
+
 /* ---- flux3_block_fwd without a caller-provided workspace.
  * This entry point has no counterpart in the model description; it is a service for
  * callers that cannot allocate device memory: for example a host program that hands all
@@ -335,7 +382,7 @@ enum {
     FLUX3_KERNEL_ROPE = 1, FLUX3_KERNEL_ADALN = 2, FLUX3_KERNEL_IN_PROJ = 3,
     FLUX3_KERNEL_ATTN = 4, FLUX3_KERNEL_OUT_PROJ = 5, FLUX3_KERNEL_FINAL = 6,
     FLUX3_KERNEL_EULER = 7, FLUX3_KERNEL_ATTN_F32 = 8, FLUX3_KERNEL_LINEAR = 9, FLUX3_KERNEL_CFG_EULER = 10,
-    FLUX3_KERNEL_TO_BF16 = 11
+    FLUX3_KERNEL_TO_BF16 = 11, FLUX3_KERNEL_QUANTIZE = 12
 };
 flux3_status flux3_profile_begin(int32_t capacity);
 flux3_status flux3_profile_end(float *ms, int32_t *kinds, int32_t capacity, int32_t *n);
