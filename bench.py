@@ -36,12 +36,14 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=["joint", "stage1", "joint_ref", "refs10", "refs10_s1", "dit", "loop"],
+    p.add_argument("--workload", choices=["joint", "joint_fp8", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
+                                          "loop"],
                    default="joint",
                    help="joint: the headline 4,256-token joint block.  The others print one line each for "
                         "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
                         "(4096+4096+160 tokens), refs10 / refs10_s1 (image + ten references + text = 45,216 "
-                        "tokens, joint / per-stream block), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
+                        "tokens, joint / per-stream block), joint_fp8 (the 4,256-token joint block with the e4m3 input "
+                        "projection), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
                         "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager and as a CUDA graph)")
     return p.parse_args()
 
@@ -432,8 +434,10 @@ def run_workload(args):
     stream = torch.cuda.current_stream()
     out = {"impl": "ours", "workload": args.workload, "n_gpus": 1, "data": "synthetic", "dtype": "bf16",
            "higher_is_better": True, "unit": "tokens/s"}
-    if args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1"):
-        if args.workload.startswith("refs10"):
+    if args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1", "joint_fp8"):
+        if args.workload == "joint_fp8":
+            case = synth.config(1)
+        elif args.workload.startswith("refs10"):
             case = synth.config_refs(10, 1 if args.workload == "refs10_s1" else 2, seed=5)
         else:
             case = synth.config(2 if args.workload == "stage1" else 3)
@@ -451,9 +455,15 @@ def run_workload(args):
         x_out = torch.empty_like(x)
         wsp = B.workspace(B.block_workspace_size(d, N), dev)
 
+        w8 = B.Fp8Weights(ws_[0]) if args.workload == "joint_fp8" else None
+        if w8 is not None:
+            wsp = B.workspace(B.block_fp8_workspace_size(d, N), dev)
+
         def step():
             B.rope_build(d, pos, out=rope, stream=stream)
-            if case.stage == 1:
+            if w8 is not None:
+                B.block_fp8_fwd(d, w8, case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
+            elif case.stage == 1:
                 B.stream_block_fwd(d, ws_, case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
             else:
                 B.block_fwd(d, ws_[0], case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
