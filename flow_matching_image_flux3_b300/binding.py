@@ -106,6 +106,7 @@ def _load() -> ctypes.CDLL:
         "flux3_block_fwd_static": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp,
                                            c_i32, c_vp, c_vp]),
         "flux3_device_error": (c_i32, [P(ctypes.c_uint32), c_i32]),
+        "flux3_selftest_timeout": (c_i32, [ctypes.c_uint32]),
         "flux3_profile_begin": (c_i32, [c_i32]),
         "flux3_profile_end": (c_i32, [P(c_f32), P(c_i32), c_i32, P(c_i32)]),
     }
@@ -124,7 +125,7 @@ EXPORTED = [
     "flux3_device_error", "flux3_profile_begin", "flux3_profile_end", "flux3_block_fwd_static",
     "flux3_sigma_schedule", "flux3_linear_fwd", "flux3_cfg_euler_step", "flux3_sample_workspace_size",
     "flux3_sample_fwd", "flux3_quantize_rows_fp8", "flux3_in_proj_fp8_fwd", "flux3_block_fp8_workspace_size",
-    "flux3_block_fp8_fwd",
+    "flux3_block_fp8_fwd", "flux3_selftest_timeout",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -491,6 +492,11 @@ def block_fp8_fwd(dims, weights: Fp8Weights, seg_off: Sequence[int], mod: torch.
                                                           _ptr(rope, torch.float32), _ptr(ws), ws.numel(),
                                                           _stream(stream)))
     return x_out
+
+
+def selftest_timeout(timeout_us: int) -> None:
+    """Runs the bounded-wait diagnostic (a device wait that is never satisfied)."""
+    _check("flux3_selftest_timeout", lib.flux3_selftest_timeout(timeout_us))
 
 
 def device_error(reset: bool = True) -> int:

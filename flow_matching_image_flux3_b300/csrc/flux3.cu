@@ -533,6 +533,9 @@ SampleWs sample_ws_layout(const flux3_dims* d, const flux3_sample_args* a, uint8
 
 }  // namespace
 
+// result slot of the bounded-wait diagnostic (flux3_selftest_timeout)
+static __device__ int g_selftest_result;
+
 // ---------------------------------------------------------------- static scratch
 // Scratch for flux3_block_fwd_static: one file-scope device array.  Host code may not use
 // the symbol as an address; the device address is looked up once per device.
@@ -962,6 +965,18 @@ flux3_status flux3_device_error(uint32_t* flags, int32_t reset) {
     }
     if (flags) *flags = v;
     return v ? FLUX3_ERR_TIMEOUT : FLUX3_OK;
+}
+
+flux3_status flux3_selftest_timeout(uint32_t timeout_us) {
+    if (timeout_us < 1 || timeout_us > 10u * 1000 * 1000) return FLUX3_ERR_INVALID_ARG;
+    int* d = nullptr;  // the kernel's one-int result slot: a file-scope device symbol, no allocation
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d), g_selftest_result) != cudaSuccess) return FLUX3_ERR_CUDA;
+    int h = -1;
+    selftest_wait_kernel<<<1, 32>>>(1000ull * timeout_us, d);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&h, g_selftest_result, sizeof(int));  // synchronises
+    if (e != cudaSuccess) return FLUX3_ERR_CUDA;
+    return h == 0 ? FLUX3_OK : FLUX3_ERR_CUDA;  // h == 1 would mean the barrier completed
 }
 
 flux3_status flux3_profile_begin(int32_t capacity) {

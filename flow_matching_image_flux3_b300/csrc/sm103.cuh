@@ -67,7 +67,8 @@ F3_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Bounded: gives up after
 // kWaitTimeoutNs, or at once when another thread of the CTA has given up (abort != 0),
 // setting the device error word.  Returns false when it gave up.
-F3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+F3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                      unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
@@ -75,7 +76,7 @@ F3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitTimeoutNs) {
+        if (globaltimer() - t0 > timeout_ns) {
             atomicOr(&g_device_error, kErrTimeout);
             *abort_flag = 1;
             return false;
@@ -101,9 +102,26 @@ F3_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // straight into the bounded wait loop costs about 90 even then.  (A role loop run by one
 // lane while the other 31 sit elsewhere pays about 100 cycles per check; a converged warp
 // with one elected lane issuing pays a few.)
-F3_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+F3_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                           unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, timeout_ns));
+}
+
+// Diagnostic for the timeout path every kernel relies on: one warp waits, through
+// mbar_wait_warp, on a barrier nothing ever arrives at.  The wait gives up after
+// timeout_ns, sets the device error word and the kernel returns normally.
+__global__ void selftest_wait_kernel(unsigned long long timeout_ns, int* result) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_warp(smem_u32(&bar), 0, &abort_flag, timeout_ns);
+    if (threadIdx.x == 0) *result = ok ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ TMA

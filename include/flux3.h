@@ -374,6 +374,14 @@ flux3_status flux3_block_fwd_static(const flux3_dims *dims, const flux3_block_we
  * reset != 0 clears the flags.  Blocking; not for the hot path. */
 flux3_status flux3_device_error(uint32_t *flags, int32_t reset);
 
+/* Diagnostic (not part of the model): exercises the bounded-wait path every kernel uses.
+ * Launches one warp that waits on a device barrier nothing ever completes; after
+ * timeout_us microseconds (1 .. 10,000,000) the wait gives up, sets the device error flag
+ * that flux3_device_error reports as FLUX3_ERR_TIMEOUT, and the kernel returns normally:
+ * the CUDA context stays usable.  Synchronises; returns FLUX3_OK when the wait timed
+ * out as designed (the flag is left set for flux3_device_error to read and reset). */
+flux3_status flux3_selftest_timeout(uint32_t timeout_us);
+
 /* Kernel timing for measurement.  Between begin and end, every kernel launch is
  * bracketed by two CUDA events on its stream (at most `capacity` launches are
  * recorded).  flux3_profile_end synchronises, writes each launch's duration in ms and

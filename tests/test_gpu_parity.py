@@ -370,3 +370,16 @@ def test_euler_step():
     d = lat.cuda()
     B.euler_step(d, v.cuda(), 0.8, 0.75)
     np.testing.assert_allclose(f64(d), O.euler_step(f64(lat), f64(v), 0.8, 0.75), rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------------------ the bounded-wait failure path
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    # a device wait on a barrier nothing completes: it must give up after its limit, set
+    # the error flag the host reads, and leave the context working
+    assert B.device_error(reset=True) == 0
+    B.selftest_timeout(20000)                      # 20 ms
+    assert B.device_error(reset=True) == 1         # bit 0: a bounded wait ran out
+    assert B.device_error(reset=True) == 0         # reset
+    case = synth.config(0, bias=True)
+    out = _run_block(case)
+    assert_close("x_out after a timed-out wait", f64(out), oracle_block(case).x_out)
