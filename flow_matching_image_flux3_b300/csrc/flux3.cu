@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -74,12 +75,12 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
 // (one flag array per kernel: the kernel is the template argument)
 template <auto Kernel>
 bool smem_attr_once(int bytes) {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64] = {};  // host threads may launch concurrently
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (done[dev]) return true;
+    if (done[dev].load(std::memory_order_acquire)) return true;
     if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
-    done[dev] = true;
+    done[dev].store(true, std::memory_order_release);  // setting it twice is harmless
     return true;
 }
 
@@ -209,10 +210,11 @@ flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& 
 // paired within a GPC, so this can be below half the SM count); cached per device.
 template <int BN, int EPI, int AK>
 int max_active_pairs(int smem, int sms) {
-    static int cache[64] = {};
+    static std::atomic<int> cache[64] = {};  // host threads may launch concurrently
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] > 0) return cache[dev];
+    const int known = cache[dev].load(std::memory_order_acquire);
+    if (known > 0) return known;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(sms & ~1));
     cfg.blockDim = dim3(GEMM_THREADS);
@@ -226,7 +228,7 @@ int max_active_pairs(int smem, int sms) {
     cfg.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<BN, EPI, 2, AK>, &cfg) != cudaSuccess) return 0;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_release);
     return n;
 }
 
