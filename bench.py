@@ -32,8 +32,9 @@ WORKLOAD = "FLUX.3 Image Klein stage-2 joint block, 1024x1024 image (4096 tok) +
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: per workload, about half a minute of timed work)")
+    p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", choices=["joint", "joint_fp8", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
@@ -45,7 +46,19 @@ def parse():
                         "tokens, joint / per-stream block), joint_fp8 (the 4,256-token joint block with the e4m3 input "
                         "projection), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
                         "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager and as a CUDA graph)")
-    return p.parse_args()
+    args = p.parse_args()
+    steps, warmup = DEFAULT_STEPS[args.workload]
+    if args.impl == "reference":
+        steps, warmup = 1000, 20
+    args.steps = steps if args.steps is None else args.steps
+    args.warmup = warmup if args.warmup is None else args.warmup
+    return args
+
+
+# Default (timed steps, warm-up steps) per workload: about half a minute of timed work each
+# (a sampling-loop step is one whole 50-step image, ~3.5 s).
+DEFAULT_STEPS = {"joint": (1000, 20), "joint_fp8": (1000, 20), "stage1": (1000, 20), "joint_ref": (1000, 20),
+                 "refs10": (100, 5), "refs10_s1": (100, 5), "dit": (200, 5), "loop": (3, 1)}
 
 
 def block_flops(D, F, n):
@@ -58,8 +71,8 @@ def block_flops(D, F, n):
 # DRAM traffic of one in_proj launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
 # ncu capture summarised in profiles/joint_block_4256_ncu_full.md; reported only while the
 # kernel sources are the ones that capture measured.
-IN_PROJ_TRAFFIC_BYTES = (203.685376 + 140.628224) * 1e6
-IN_PROJ_SOURCES = {"gemm.cuh": "7900b66b31a42051", "sm103.cuh": "b44b224cb54cb3df", "flux3.cu": "dc91de8912b1118c"}
+IN_PROJ_TRAFFIC_BYTES = (203.328000 + 140.620800) * 1e6
+IN_PROJ_SOURCES = {"gemm.cuh": "d9922c202fae3d42", "sm103.cuh": "505ea2de50cad3d3", "flux3.cu": "ff0901d8a9fae7eb"}
 
 
 def in_proj_traffic():
