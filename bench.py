@@ -38,14 +38,15 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", choices=["joint", "joint_fp8", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
-                                          "loop"],
+                                          "loop", "loop_ref"],
                    default="joint",
                    help="joint: the headline 4,256-token joint block.  The others print one line each for "
                         "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
                         "(4096+4096+160 tokens), refs10 / refs10_s1 (image + ten references + text = 45,216 "
                         "tokens, joint / per-stream block), joint_fp8 (the 4,256-token joint block with the e4m3 input "
                         "projection), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
-                        "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager and as a CUDA graph)")
+                        "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager without and with the "
+                        "context cache, and as a CUDA graph), loop_ref (the same with one 1024x1024 reference)")
     args = p.parse_args()
     steps, warmup = DEFAULT_STEPS[args.workload]
     if args.impl == "reference":
@@ -56,9 +57,10 @@ def parse():
 
 
 # Default (timed steps, warm-up steps) per workload: about half a minute of timed work each
-# (a sampling-loop step is one whole 50-step image, ~3.5 s).
+# (a sampling-loop step is one whole 50-step image, ~3.5 s; ~8 s with a reference).
 DEFAULT_STEPS = {"joint": (1000, 20), "joint_fp8": (1000, 20), "stage1": (1000, 20), "joint_ref": (1000, 20),
-                 "refs10": (100, 5), "refs10_s1": (100, 5), "dit": (200, 5), "loop": (3, 1)}
+                 "refs10": (100, 5), "refs10_s1": (100, 5), "dit": (200, 5), "loop": (2, 1),
+                 "loop_ref": (1, 1)}
 
 
 def block_flops(D, F, n):
@@ -496,13 +498,15 @@ def run_workload(args):
                     "config": {"tokens": N, "segments": segs, "stage": case.stage, "flops_per_step": flops},
                     "kernels_avg_ms": {k: sum(v) / len(v) for k, v in per.items()}})
     else:
-        # the denoiser: 5 stage-1 blocks (image | text, own weights each), 28 joint blocks, output
-        # layer 3072 -> 128 on image rows; 1024x1024 text-to-image: 4,096 image + 160 text tokens.
-        # Weights ~ N(0, 1/fan_in) drawn on the device (seeded); 9.3 GB.
+        # the denoiser: 5 stage-1 blocks (image | [reference |] text, own weights each), 28 joint
+        # blocks, output layer 3072 -> 128 on image rows; 1024x1024 text-to-image: 4,096 image +
+        # 160 text tokens (loop_ref: + one 1024x1024 reference, 4,096 tokens at t = 1).
+        # Weights ~ N(0, 1/fan_in) drawn on the device (seeded); 9.3 GB (10.5 GB with a reference).
         d = synth.FULL
         D, F, H = d.width, d.ffn_hidden, d.heads
-        n_img, n_txt = 4096, 160
-        N = n_img + n_txt
+        n_img, n_ref, n_txt = 4096, (4096 if args.workload == "loop_ref" else 0), 160
+        N = n_img + n_ref + n_txt
+        ns = 3 if n_ref else 2
         g = torch.Generator(device=dev).manual_seed(4)
 
         def rnd(shape, std, dtype=torch.bfloat16):
@@ -515,7 +519,7 @@ def run_workload(args):
                 self.k_norm = 1 + rnd((128,), 0.1, torch.float32)
                 self.w_out, self.b_out = rnd((D, D + F), (D + F) ** -0.5), None
         n_s1, n_j = 5, 28
-        stage1 = [[DW(), DW()] for _ in range(n_s1)]
+        stage1 = [[DW() for _ in range(ns)] for _ in range(n_s1)]
         joint = [DW() for _ in range(n_j)]
         w_final = rnd((128, D), D ** -0.5)
 
@@ -526,16 +530,22 @@ def run_workload(args):
                 t[..., 2, :].normal_(0, 0.5, generator=g)
                 return t
             fin = torch.empty(2, D, device=dev).normal_(0, 0.1, generator=g)
-            return m(n_s1, 2), m(n_j, 2), fin
-        dargs = [B.DitArgs(stage1, joint, w_final, None, *mods(), 2)]
-        streams = [synth.image_stream(1024, 1024), synth.text_stream(n_txt)]
+            return m(n_s1, ns), m(n_j, ns), fin
+        dargs = [B.DitArgs(stage1, joint, w_final, None, *mods(), ns)]
+        streams = [synth.image_stream(1024, 1024)]
+        if n_ref:
+            streams.append(synth.Stream("ref", n_ref, (64, 64), t=1))
+        streams.append(synth.text_stream(n_txt))
         pos = synth.positions(streams).to(dev)
         base = rnd((N, D), 1.0)
         tok = torch.empty_like(base)
         vel = torch.empty(n_img, 128, dtype=torch.float32, device=dev)
-        wsp = B.workspace(B.dit_workspace_size(d, n_img, 0, n_txt), dev)
-        fwd_flops = n_s1 * (sum(block_flops(D, F, n)[0] + block_flops(D, F, n)[2] + 4.0 * n * n * D
-                                for n in (n_img, n_txt))) + n_j * sum(block_flops(D, F, N)) + 2.0 * n_img * D * 128
+        wsp = B.workspace(B.dit_workspace_size(d, n_img, n_ref, n_txt), dev)
+
+        def stage1_flops(n):
+            return n_s1 * (block_flops(D, F, n)[0] + block_flops(D, F, n)[2] + 4.0 * n * n * D) if n else 0.0
+        ctx_flops = stage1_flops(n_ref) + stage1_flops(n_txt)
+        fwd_flops = stage1_flops(n_img) + ctx_flops + n_j * sum(block_flops(D, F, N)) + 2.0 * n_img * D * 128
 
         def forward():
             tok.copy_(base)  # the stack works in place on the token buffer
@@ -551,27 +561,36 @@ def run_workload(args):
         else:
             # the base-model loop through flux3_sample_fwd: 50 steps with guidance 3.5 (two
             # denoiser calls per step), embedders 128 -> 3072 and 20,480 -> 3072, the prompt's
-            # and the negative prompt's text features embedded once per image
+            # and the negative prompt's text features (and the reference) embedded once per
+            # image.  Timed without and with the context cache (the reference and text
+            # streams' stage 1 once per prompt); their stage-1 modulation is the same at
+            # every step, as the cache requires.
             T = 20480
             w_img, b_img = rnd((D, 128), 128 ** -0.5), None
             w_txt, b_txt = rnd((D, T), T ** -0.5), None
             t_pos, t_neg = rnd((n_txt, T), 1.0), rnd((n_txt, T), 1.0)
+            ref_lat = rnd((n_ref, 128), 1.0) if n_ref else None
             cfg_scale = 3.5
             step_mods = [mods() for _ in range(50)]
-            sargs = B.SampleArgs(n_img, 0, n_txt, w_img, b_img, w_txt, b_txt, t_pos, t_neg, pos, step_mods, 50,
-                                 6.93, cfg_scale)
-            sws = B.workspace(B.sample_workspace_size(d, sargs), dev)
+            for m in step_mods[1:]:
+                m[0][:, 1:].copy_(step_mods[0][0][:, 1:])
             lat0 = torch.randn(n_img, 128, generator=g, device=dev)
             lat = lat0.clone()
+            timings = {}
+            for cache in (False, True):
+                sargs = B.SampleArgs(n_img, n_ref, n_txt, w_img, b_img, w_txt, b_txt, t_pos, t_neg, pos, step_mods, 50,
+                                     6.93, cfg_scale, ref_latent=ref_lat, cache_context=cache)
+                sws = B.workspace(B.sample_workspace_size(d, sargs), dev)
 
-            def image():
-                lat.copy_(lat0)
-                B.sample_fwd(d, dargs[0], sargs, lat, ws=sws, stream=stream)
-            ms = _timed(image, max(1, args.steps), 1, stream)
+                def image():
+                    lat.copy_(lat0)
+                    B.sample_fwd(d, dargs[0], sargs, lat, ws=sws, stream=stream)
+                timings[cache] = _timed(image, max(1, args.steps), max(1, args.warmup), stream)
+            ms = timings[True]
             graph_ms, graph_err = None, None
             try:
-                # the whole 50-step call captured once and replayed (the library allocates
-                # nothing and launches only on the caller's stream)
+                # the whole 50-step call (context cached) captured once and replayed (the
+                # library allocates nothing and launches only on the caller's stream)
                 gr = torch.cuda.CUDAGraph()
                 side = torch.cuda.Stream()
                 side.wait_stream(stream)
@@ -586,12 +605,16 @@ def run_workload(args):
             except Exception as e:  # report, do not hide, a capture failure
                 graph_err = f"{type(e).__name__}: {e}"
             img_flops = 50 * 2 * fwd_flops
+            cached_flops = 50 * 2 * (fwd_flops - ctx_flops) + 2 * ctx_flops
             out.update({"metric": "50-step guided sampling loop, images/s (1024x1024)", "value": 1e3 / ms,
-                        "unit": "images/s", "ms_per_image": ms, "tflops": img_flops / (ms / 1e3) / 1e12,
+                        "unit": "images/s", "ms_per_image": ms, "tflops": cached_flops / (ms / 1e3) / 1e12,
+                        "uncached_ms_per_image": timings[False],
+                        "uncached_tflops": img_flops / (timings[False] / 1e3) / 1e12,
                         "graph_ms_per_image": graph_ms, "graph_error": graph_err, "steps": max(1, args.steps),
-                        "config": {"tokens": N, "steps_per_image": 50, "cfg_scale": cfg_scale,
-                                   "denoiser_calls_per_image": 100, "flops_per_image": img_flops,
-                                   "alpha": 6.93}})
+                        "config": {"tokens": N, "reference_tokens": n_ref, "steps_per_image": 50,
+                                   "cfg_scale": cfg_scale, "denoiser_calls_per_image": 100,
+                                   "context_cached": True, "flops_per_image": cached_flops,
+                                   "flops_per_image_uncached": img_flops, "alpha": 6.93}})
     assert B.device_error() == 0
     print(json.dumps(out), flush=True)
 

@@ -55,7 +55,7 @@ class flux3_sample_args(ctypes.Structure):
     _fields_ = [("n_img", c_i32), ("n_ref", c_i32), ("n_txt", c_i32), ("latent_channels", c_i32), ("text_dim", c_i32),
                 ("w_img", c_vp), ("b_img", c_vp), ("w_txt", c_vp), ("b_txt", c_vp), ("ref_latent", c_vp),
                 ("text_pos", c_vp), ("text_neg", c_vp), ("pos", c_vp), ("mod", ctypes.POINTER(flux3_dit_mod)),
-                ("n_steps", c_i32), ("alpha", c_f32), ("cfg_scale", c_f32)]
+                ("n_steps", c_i32), ("alpha", c_f32), ("cfg_scale", c_f32), ("cache_context", c_i32)]
 
 
 class Flux3Error(RuntimeError):
@@ -400,7 +400,8 @@ class SampleArgs:
     def __init__(self, n_img: int, n_ref: int, n_txt: int, w_img: torch.Tensor, b_img: Optional[torch.Tensor],
                  w_txt: torch.Tensor, b_txt: Optional[torch.Tensor], text_pos: torch.Tensor,
                  text_neg: Optional[torch.Tensor], pos: torch.Tensor, step_mods: Sequence, n_steps: int,
-                 alpha: float, cfg_scale: float, ref_latent: Optional[torch.Tensor] = None):
+                 alpha: float, cfg_scale: float, ref_latent: Optional[torch.Tensor] = None,
+                 cache_context: bool = False):
         # step_mods: one (mod_stage1, mod_joint, mod_final) device tuple per step
         self._keep = [w_img, b_img, w_txt, b_txt, text_pos, text_neg, pos, step_mods, ref_latent]
         self.mods = (flux3_dit_mod * n_steps)(*[flux3_dit_mod(_ptr(m[0], torch.float32), _ptr(m[1], torch.float32),
@@ -409,7 +410,8 @@ class SampleArgs:
                                    _ptr(b_img, torch.float32), _ptr(w_txt, torch.bfloat16), _ptr(b_txt, torch.float32),
                                    _ptr(ref_latent, torch.bfloat16), _ptr(text_pos, torch.bfloat16),
                                    _ptr(text_neg, torch.bfloat16), _ptr(pos, torch.int32),
-                                   ctypes.cast(self.mods, ctypes.POINTER(flux3_dit_mod)), n_steps, alpha, cfg_scale)
+                                   ctypes.cast(self.mods, ctypes.POINTER(flux3_dit_mod)), n_steps, alpha, cfg_scale,
+                                   int(bool(cache_context)))
 
 
 def sample_workspace_size(dims, args: SampleArgs) -> int:

@@ -701,6 +701,72 @@ flux3_status flux3_final_fwd(const flux3_dims* dims, const void* w_final, const 
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Row offsets of the denoiser's streams in the token buffer: image | [reference] | text.
+struct DitStreams {
+    int n;          // 2 or 3
+    int32_t off[4];  // off[i] .. off[i + 1]: the rows of stream i
+};
+DitStreams dit_streams(int ns, int n_img, int n_ref, int n_txt) {
+    DitStreams d;
+    d.n = ns;
+    d.off[0] = 0;
+    d.off[1] = n_img;
+    d.off[2] = ns == 3 ? n_img + n_ref : n_img + n_txt;
+    d.off[3] = ns == 3 ? n_img + n_ref + n_txt : 0;
+    return d;
+}
+
+// The denoiser's weights: counts, pointers and the output layer's shape.
+flux3_status check_dit(const flux3_dims* d, const flux3_dit_weights* w) {
+    (void)d;
+    if (w->n_streams < 2 || w->n_streams > 3) return FLUX3_ERR_INVALID_ARG;
+    if (w->n_stage1 < 0 || w->n_joint < 0 || (w->n_stage1 > 0 && !w->stage1) || (w->n_joint > 0 && !w->joint))
+        return FLUX3_ERR_INVALID_ARG;
+    if (w->out_channels <= 0 || w->out_channels > 4096) return FLUX3_ERR_INVALID_ARG;
+    if (w->out_channels % 128 != 0) return FLUX3_ERR_UNSUPPORTED;
+    flux3_status s;
+    for (int i = 0; i < w->n_stage1; ++i)
+        if ((s = check_weights(w->stage1 + (size_t)i * w->n_streams, w->n_streams, true, true)) != FLUX3_OK) return s;
+    for (int i = 0; i < w->n_joint; ++i)
+        if ((s = check_weights(w->joint + i, 1, true, true)) != FLUX3_OK) return s;
+    return FLUX3_OK;
+}
+
+// Stage 1 (each stream through its own blocks, attention within the stream) for streams
+// s0 .. s1-1, whose rows start at x (bf16, updated in place); rope holds the table rows
+// of those tokens.  mod_stage1 is the denoiser's [n_stage1][n_streams][3][D] array.
+flux3_status dit_stage1(const flux3_dims* d, const flux3_dit_weights* w, const float* mod_stage1, const DitStreams& ds,
+                        int s0, int s1, void* x, const float* rope, void* bws, size_t bws_bytes, cudaStream_t st) {
+    const int n_seg = s1 - s0, N = ds.off[s1] - ds.off[s0];
+    if (n_seg <= 0 || N == 0) return FLUX3_OK;
+    int32_t loc[FLUX3_MAX_SEGMENTS + 1];
+    for (int i = 0; i <= n_seg; ++i) loc[i] = ds.off[s0 + i] - ds.off[s0];
+    const size_t mstride = (size_t)ds.n * 3 * d->width;
+    for (int b = 0; b < w->n_stage1; ++b) {
+        flux3_segments sg{n_seg, loc, mod_stage1 + b * mstride + (size_t)s0 * 3 * d->width};
+        const flux3_status s =
+            run_block(d, w->stage1 + (size_t)b * ds.n + s0, n_seg, &sg, x, x, N, rope, bws, bws_bytes, st, true);
+        if (s != FLUX3_OK) return s;
+    }
+    return FLUX3_OK;
+}
+
+// Stage 2 (the joint blocks over all tokens) and the output layer on the image rows.
+flux3_status dit_stage2(const flux3_dims* d, const flux3_dit_weights* w, const flux3_dit_mod* mod, const DitStreams& ds,
+                        void* tokens, const float* rope, float* velocity, void* bws, size_t bws_bytes, cudaStream_t st) {
+    const int N = ds.off[ds.n];
+    const size_t mstride = (size_t)ds.n * 3 * d->width;
+    for (int b = 0; b < w->n_joint; ++b) {
+        flux3_segments sg{ds.n, ds.off, mod->joint + b * mstride};
+        const flux3_status s = run_block(d, w->joint + b, 1, &sg, tokens, tokens, N, rope, bws, bws_bytes, st, false);
+        if (s != FLUX3_OK) return s;
+    }
+    return run_final(d, w->w_final, w->b_final, w->out_channels, mod->final, tokens, ds.off[1], velocity, bws, bws_bytes,
+                     st);
+}
+}  // namespace
+
 size_t flux3_dit_workspace_size(const flux3_dims* dims, int32_t n_img, int32_t n_ref, int32_t n_txt) {
     if (check_dims(dims) != FLUX3_OK || n_img < 0 || n_ref < 0 || n_txt < 0) return 0;
     const long long N = (long long)n_img + n_ref + n_txt;
@@ -718,44 +784,20 @@ flux3_status flux3_dit_fwd(const flux3_dims* dims, const flux3_dit_weights* w, c
     if (NN > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
     const int N = (int)NN;
     if (w->n_streams != (n_ref > 0 ? 3 : 2)) return FLUX3_ERR_INVALID_ARG;
-    if (w->n_stage1 < 0 || w->n_joint < 0 || (w->n_stage1 > 0 && (!w->stage1 || !mod->stage1)) ||
-        (w->n_joint > 0 && (!w->joint || !mod->joint)))
-        return FLUX3_ERR_INVALID_ARG;
-    if (w->out_channels <= 0 || w->out_channels > 4096) return FLUX3_ERR_INVALID_ARG;
-    if (w->out_channels % 128 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if ((w->n_stage1 > 0 && !mod->stage1) || (w->n_joint > 0 && !mod->joint)) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_dit(dims, w)) != FLUX3_OK) return s;
     if (N == 0) return FLUX3_OK;
     if (!tokens || !pos || !velocity || !w->w_final || !mod->final) return FLUX3_ERR_INVALID_ARG;
     if (!al16(tokens) || !al16(pos) || !al16(velocity)) return FLUX3_ERR_INVALID_ARG;
-    for (int i = 0; i < w->n_stage1; ++i)
-        if ((s = check_weights(w->stage1 + (size_t)i * w->n_streams, w->n_streams, true, true)) != FLUX3_OK) return s;
-    for (int i = 0; i < w->n_joint; ++i)
-        if ((s = check_weights(w->joint + i, 1, true, true)) != FLUX3_OK) return s;
     if (!ws || !al256(ws) || ws_bytes < flux3_dit_workspace_size(dims, n_img, n_ref, n_txt)) return FLUX3_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* rope = static_cast<float*>(ws);
     uint8_t* bws = static_cast<uint8_t*>(ws) + up256((size_t)N * 128 * 4);
     const size_t bws_bytes = ws_bytes - up256((size_t)N * 128 * 4);
     if ((s = flux3_rope_build(dims, pos, N, rope, stream)) != FLUX3_OK) return s;
-    int32_t off[4] = {0, n_img, 0, 0};
-    int ns = w->n_streams;
-    if (ns == 3) {
-        off[2] = n_img + n_ref;
-        off[3] = N;
-    } else {
-        off[2] = N;
-    }
-    const size_t mstride = (size_t)ns * 3 * dims->width;
-    for (int b = 0; b < w->n_stage1; ++b) {
-        flux3_segments sg{ns, off, mod->stage1 + b * mstride};
-        if ((s = run_block(dims, w->stage1 + (size_t)b * ns, ns, &sg, tokens, tokens, N, rope, bws, bws_bytes, st, true)) !=
-            FLUX3_OK)
-            return s;
-    }
-    for (int b = 0; b < w->n_joint; ++b) {
-        flux3_segments sg{ns, off, mod->joint + b * mstride};
-        if ((s = run_block(dims, w->joint + b, 1, &sg, tokens, tokens, N, rope, bws, bws_bytes, st, false)) != FLUX3_OK) return s;
-    }
-    return run_final(dims, w->w_final, w->b_final, w->out_channels, mod->final, tokens, n_img, velocity, bws, bws_bytes, st);
+    const DitStreams ds = dit_streams(w->n_streams, n_img, n_ref, n_txt);
+    if ((s = dit_stage1(dims, w, mod->stage1, ds, 0, ds.n, tokens, rope, bws, bws_bytes, st)) != FLUX3_OK) return s;
+    return dit_stage2(dims, w, mod, ds, tokens, rope, velocity, bws, bws_bytes, st);
 }
 
 flux3_status flux3_block_fwd_static(const flux3_dims* dims, const flux3_block_weights* w, const flux3_segments* segs,
@@ -841,8 +883,12 @@ flux3_status flux3_sample_fwd(const flux3_dims* dims, const flux3_dit_weights* w
     if (s != FLUX3_OK) return s;
     if (!w || w->out_channels != a->latent_channels) return FLUX3_ERR_INVALID_ARG;
     if (w->n_streams != (a->n_ref > 0 ? 3 : 2)) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_dit(dims, w)) != FLUX3_OK) return s;
+    for (int i = 0; i < a->n_steps; ++i)
+        if ((w->n_stage1 > 0 && !a->mod[i].stage1) || (w->n_joint > 0 && !a->mod[i].joint) || !a->mod[i].final)
+            return FLUX3_ERR_INVALID_ARG;
     if (a->n_img == 0) return FLUX3_OK;
-    if (!latent || !al16(latent)) return FLUX3_ERR_INVALID_ARG;
+    if (!latent || !al16(latent) || !w->w_final) return FLUX3_ERR_INVALID_ARG;
     const SampleWs need = sample_ws_layout(dims, a, nullptr);
     if (!ws || !al256(ws) || ws_bytes < need.bytes) return FLUX3_ERR_WORKSPACE;
     if (!have_encode()) return FLUX3_ERR_CUDA;
@@ -866,6 +912,22 @@ flux3_status flux3_sample_fwd(const flux3_dims* dims, const flux3_dit_weights* w
     to_bf16_kernel<<<(unsigned)((n_lat + 255) / 256), 256, 0, st>>>(latent, n_lat, b.lat_bf);
     prof_after(st);
     if ((s = launch_status()) != FLUX3_OK) return s;
+    const bool cache = a->cache_context != 0 && ctx_bytes > 0 && w->n_stage1 > 0;
+    const DitStreams ds = dit_streams(w->n_streams, a->n_img, a->n_ref, a->n_txt);
+    const int N = ds.off[ds.n];
+    float* rope = reinterpret_cast<float*>(b.dit);
+    uint8_t* bws = b.dit + up256((size_t)N * 128 * 4);
+    const size_t bws_bytes = b.dit_bytes - up256((size_t)N * 128 * 4);
+    if (cache) {
+        // The reference and text streams see the same modulation at every step (step 0's)
+        // and attend only to themselves in stage 1, so their stage-1 output does not
+        // depend on the step: compute it once per prompt, in place in the context buffers.
+        if ((s = flux3_rope_build(dims, a->pos, N, rope, stream)) != FLUX3_OK) return s;
+        for (int k = 0; k < (cfg ? 2 : 1); ++k)
+            if ((s = dit_stage1(dims, w, a->mod[0].stage1, ds, 1, ds.n, k == 0 ? b.ctx_pos : b.ctx_neg,
+                                rope + (size_t)a->n_img * 128, bws, bws_bytes, st)) != FLUX3_OK)
+                return s;
+    }
     for (int i = 0; i < a->n_steps; ++i) {
         for (int k = 0; k < (cfg ? 2 : 1); ++k) {
             // the denoiser overwrites the token buffer: rebuild it for every call
@@ -874,8 +936,15 @@ flux3_status flux3_sample_fwd(const flux3_dims* dims, const flux3_dit_weights* w
                 cudaMemcpyAsync(b.tokens + (size_t)a->n_img * D, k == 0 ? b.ctx_pos : b.ctx_neg, ctx_bytes,
                                 cudaMemcpyDeviceToDevice, st) != cudaSuccess)
                 return FLUX3_ERR_CUDA;
-            if ((s = flux3_dit_fwd(dims, w, &a->mod[i], b.tokens, a->n_img, a->n_ref, a->n_txt, a->pos,
-                                   k == 0 ? b.v_pos : b.v_neg, b.dit, b.dit_bytes, stream)) != FLUX3_OK)
+            float* v = k == 0 ? b.v_pos : b.v_neg;
+            if (!cache) {
+                if ((s = flux3_dit_fwd(dims, w, &a->mod[i], b.tokens, a->n_img, a->n_ref, a->n_txt, a->pos, v, b.dit,
+                                       b.dit_bytes, stream)) != FLUX3_OK)
+                    return s;
+                continue;
+            }
+            if ((s = dit_stage1(dims, w, a->mod[i].stage1, ds, 0, 1, b.tokens, rope, bws, bws_bytes, st)) != FLUX3_OK ||
+                (s = dit_stage2(dims, w, &a->mod[i], ds, b.tokens, rope, v, bws, bws_bytes, st)) != FLUX3_OK)
                 return s;
         }
         if ((s = run_cfg_euler(latent, b.v_pos, cfg ? b.v_neg : nullptr, n_lat, a->cfg_scale, sig[i + 1] - sig[i], b.lat_bf,

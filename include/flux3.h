@@ -282,6 +282,8 @@ typedef struct flux3_sample_args {
     int32_t n_steps;              /* >= 1 (50 for the base checkpoint)                          */
     float alpha;                  /* rational time shift (6.93)                                 */
     float cfg_scale;              /* 1 = no guidance (one denoiser call per step), else two     */
+    int32_t cache_context;        /* nonzero: run the stage-1 blocks of the reference and text
+                                     streams once per prompt instead of once per step (below)  */
 } flux3_sample_args;
 
 /* Workspace of flux3_sample_fwd in bytes (0 for invalid arguments). */
@@ -291,6 +293,14 @@ size_t flux3_sample_workspace_size(const flux3_dims *dims, const flux3_sample_ar
  * append the embedded references and text (embedded once per call), run the denoiser
  * for the prompt (and with guidance again for the negative prompt), and take the guided
  * Euler step from sigmas[i] to sigmas[i + 1] (flux3_sigma_schedule).
+ * cache_context: the reference and text streams get the modulation vector of timestep 0
+ * at every step ("Welcome FLUX.3 Image Klein in Diffusers", section "How it works": text
+ * and references are clean inputs), and in stage 1 a stream attends only to itself, so
+ * their stage-1 outputs are the same at every step.  With cache_context set the loop
+ * runs those streams' stage-1 blocks once per prompt, with the stage-1 modulation of
+ * step 0 (mod[0].stage1, the reference and text entries), and reuses the result; the
+ * caller asserts that these entries are the same at every step.  The result then equals
+ * the uncached loop's up to fp32 summation order inside the stage-1 GEMMs. 
  * latent  device fp32 [n_img, latent_channels], updated in place (in: the initial noise,
  *         out: the sample).  The denoiser's out_channels must equal latent_channels;
  *         n_ref > 0 requires a 3-stream denoiser, n_ref == 0 a 2-stream one. */

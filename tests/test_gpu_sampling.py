@@ -59,7 +59,11 @@ def test_cfg_euler_step(guided):
     assert torch.equal(lb.cpu(), dl.cpu().to(torch.bfloat16))   # the bf16 copy of the new latent
 
 
-def _tiny_loop(n_ref, n_steps, cfg_scale, seed=91):
+def _tiny_loop(n_ref, n_steps, cfg_scale, seed=91, cache=None):
+    """The loop on the device and in the oracle.  cache=None: per-step modulation for every
+    stream, uncached loop.  cache=True/False: the stage-1 reference and text entries are
+    step 0's at every step (the clean-context reading) and the device loop runs with
+    cache_context set/cleared.  Returns (device latent, oracle latent, initial latent)."""
     dims = synth.TINY
     D = dims.width
     g = gen(seed)
@@ -87,6 +91,9 @@ def _tiny_loop(n_ref, n_steps, cfg_scale, seed=91):
     mods = [(torch.stack([synth.draw_mod(g, ns, D) for _ in range(2)]),
              torch.stack([synth.draw_mod(g, ns, D) for _ in range(2)]),
              torch.randn(2, D, generator=g) * 0.1) for _ in range(n_steps)]
+    if cache is not None:
+        for m in mods[1:]:
+            m[0][:, 1:] = mods[0][0][:, 1:]
     lat0 = torch.randn(n_img, C, generator=g)
 
     # ---- device, through flux3_sample_fwd
@@ -95,7 +102,7 @@ def _tiny_loop(n_ref, n_steps, cfg_scale, seed=91):
     dit = B.DitArgs(keep["s1"], keep["j"], wf.cuda(), bf.cuda(), dmods[0][0], dmods[0][1], dmods[0][2], ns)
     args = B.SampleArgs(n_img, n_ref, n_txt, w_img.cuda(), b_img.cuda(), w_txt.cuda(), b_txt.cuda(), t_pos.cuda(),
                         t_neg.cuda() if cfg_scale != 1.0 else None, pos.cuda(), dmods, n_steps, 6.93, cfg_scale,
-                        ref_latent=ref.cuda() if n_ref else None)
+                        ref_latent=ref.cuda() if n_ref else None, cache_context=bool(cache))
     lat = lat0.cuda()
     B.sample_fwd(dims, dit, args, lat)
     torch.cuda.synchronize()
@@ -139,3 +146,15 @@ def test_sampling_loop_tiny(n_ref, n_steps, cfg_scale):
     assert_close("latent after the loop", got, ref, rl2=REL_L2, ma=LOOP_MAX_ABS)
     # the loop moved the latent by far more than the tolerance (the comparison is not vacuous)
     assert np.linalg.norm(ref - lat0) > 10 * REL_L2 * np.linalg.norm(ref)
+
+
+@pytest.mark.parametrize("n_ref,n_steps,cfg_scale", [(0, 3, 3.5), (64, 2, 3.5), (64, 2, 1.0)])
+def test_sampling_loop_cached_context(n_ref, n_steps, cfg_scale):
+    """The loop that runs the context streams' stage 1 once per prompt against the oracle
+    loop (which recomputes every stream at every step) and against the uncached device
+    loop on the same inputs."""
+    got, ref, lat0 = _tiny_loop(n_ref, n_steps, cfg_scale, cache=True)
+    assert_close("latent after the cached loop", got, ref, rl2=REL_L2, ma=LOOP_MAX_ABS)
+    assert np.linalg.norm(ref - lat0) > 10 * REL_L2 * np.linalg.norm(ref)
+    plain, _, _ = _tiny_loop(n_ref, n_steps, cfg_scale, cache=False)
+    assert_close("cached vs uncached loop", got, plain, rl2=REL_L2, ma=LOOP_MAX_ABS)

@@ -76,3 +76,33 @@ def test_loop_integrates_the_straight_flow_exactly(cfg_scale):
         assert calls == [(i, True) for i in range(50)]
     else:
         assert calls == [(i, p) for i in range(50) for p in (True, False)]
+
+
+def test_context_stage1_does_not_depend_on_the_image():
+    """Welcome FLUX.3 Image Klein in Diffusers, "How it works": in stage 1 every stream runs
+    its own blocks and attends only to itself, and text (and references) get the t = 0
+    modulation at every step.  So the text rows after stage 1 are the same whatever the
+    image tokens (that is, at every sigma): bit for bit in the oracle, which is what lets
+    the sampling loop compute them once per prompt."""
+    import oracle as O
+    from flow_matching_image_flux3_b300 import synth
+    from tests.common import oracle_weights
+
+    dims = synth.TINY
+    g = torch.Generator("cpu").manual_seed(17)
+    streams = [synth.Stream("image", 64, (8, 8)), synth.text_stream(80)]
+    seg = [0, 64, 144]
+    pos = synth.positions(streams).numpy()
+    s1 = [[oracle_weights(synth.draw_weights(g, dims, True)) for _ in range(2)] for _ in range(2)]
+    m1 = [synth.as_f64(synth.draw_mod(g, 2, dims.width)) for _ in range(2)]
+    text = synth.as_f64(torch.randn(80, dims.width, generator=g).to(torch.bfloat16))
+    outs = []
+    for sigma in (0.9, 0.3):   # two image inputs, as at two noise levels
+        img = synth.as_f64(torch.randn(64, dims.width, generator=g).to(torch.bfloat16)) * sigma
+        x = np.concatenate([img, text])
+        _, h = O.dit_forward(x, seg, pos, s1, m1, [], [], np.zeros((2, dims.width)), np.zeros((128, dims.width)),
+                             np.zeros(128), heads=dims.heads, theta=1e4, rounding="bf16")
+        outs.append(h)
+    assert np.array_equal(outs[0][64:], outs[1][64:])
+    assert not np.allclose(outs[0][:64], outs[1][:64])
+    assert not np.allclose(outs[0][64:], text)    # stage 1 did change the text rows
