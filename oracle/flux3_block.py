@@ -212,25 +212,36 @@ class BlockOut:
     attn: np.ndarray; act: np.ndarray; y: np.ndarray; x_out: np.ndarray
 
 
-def _in_proj(a: np.ndarray, w: "Weights", fp8: bool) -> np.ndarray:
-    """P = a W_in^T + b_in; with fp8 the product uses row-wise e4m3 operands (oracle/fp8.py)."""
-    if fp8:
+def _in_proj(a: np.ndarray, w: "Weights", quant: Optional[str]) -> np.ndarray:
+    """P = a W_in^T + b_in; quant "fp8": the product on row-wise e4m3 operands
+    (oracle/fp8.py); "nvfp4": on NVFP4 operands (oracle/nvfp4.py)."""
+    if quant == "fp8":
         from .fp8 import fp8_linear
         return fp8_linear(a, w.w_in) + w.b_in
+    if quant == "nvfp4":
+        from .nvfp4 import nvfp4_linear
+        return nvfp4_linear(a, w.w_in) + w.b_in
+    assert quant is None
     return a @ w.w_in.T + w.b_in
+
+
+def _quant(fp8_in_proj: bool, nvfp4_in_proj: bool) -> Optional[str]:
+    assert not (fp8_in_proj and nvfp4_in_proj)
+    return "fp8" if fp8_in_proj else ("nvfp4" if nvfp4_in_proj else None)
 
 
 def block_forward(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
                   angles: np.ndarray, heads: int, head_dim: int = 128, ln_eps: float = 1e-6,
                   rms_eps: float = 1e-6, stage: int = 2, rounding: Optional[str] = None,
-                  fp8_in_proj: bool = False) -> BlockOut:
+                  fp8_in_proj: bool = False, nvfp4_in_proj: bool = False) -> BlockOut:
     """One transformer block.
 
     stage 2 (joint): one weight set, attention over all tokens, modulation per stream.
     stage 1 (per stream): weights[s] for stream s, attention inside each stream.
     rounding="bf16" rounds to bf16 where the device stores bf16 tensors (the modulated
     input, q, k, v, the attention output, the SwiGLU output and x'); None keeps fp64.
-    fp8_in_proj: the input projection on row-wise e4m3 operands (oracle/fp8.py)."""
+    fp8_in_proj: the input projection on row-wise e4m3 operands (oracle/fp8.py);
+    nvfp4_in_proj: on NVFP4 operands (oracle/nvfp4.py)."""
     x = np.asarray(x, dtype=F64)
     n, D = x.shape
     H, d = heads, head_dim
@@ -250,7 +261,7 @@ def block_forward(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int],
     q = np.empty((n, H, d)); k = np.empty((n, H, d)); v = np.empty((n, H, d))
     g = np.empty((n, F)); u = np.empty((n, F))
     for lo, hi, w in rows:
-        p = _in_proj(a[lo:hi], w, fp8_in_proj)
+        p = _in_proj(a[lo:hi], w, _quant(fp8_in_proj, nvfp4_in_proj))
         q[lo:hi] = rope_rotate(rms_norm(p[:, 0:D].reshape(-1, H, d), w.q_norm, rms_eps), angles[lo:hi])
         k[lo:hi] = rope_rotate(rms_norm(p[:, D:2 * D].reshape(-1, H, d), w.k_norm, rms_eps), angles[lo:hi])
         v[lo:hi] = p[:, 2 * D:3 * D].reshape(-1, H, d)
@@ -310,7 +321,7 @@ def euler_step(latent: np.ndarray, velocity: np.ndarray, sigma: float, sigma_nex
 def block_keys_values(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
                       angles: np.ndarray, heads: int, rows: Optional[Sequence[int]] = None, head_dim: int = 128,
                       ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
-                      rounding: Optional[str] = None, fp8_in_proj: bool = False):
+                      rounding: Optional[str] = None, fp8_in_proj: bool = False, nvfp4_in_proj: bool = False):
     """Keys and values [len(rows), H, d] of the given rows (all rows by default): the
     same steps as block_forward up to k and v, row by row (row-wise quantization keeps a
     row's projection independent of the other rows and of W_in's other rows)."""
@@ -326,7 +337,7 @@ def block_keys_values(x: np.ndarray, weights: List[Weights], seg_off: Sequence[i
         m = wsel == wi
         w = weights[wi]
         kw = Weights(w.w_in[D:3 * D], w.b_in[D:3 * D], w.q_norm, w.k_norm, w.w_out, w.b_out)
-        pkv = _in_proj(a[m], kw, fp8_in_proj)
+        pkv = _in_proj(a[m], kw, _quant(fp8_in_proj, nvfp4_in_proj))
         pk, pv = pkv[:, 0:D], pkv[:, D:2 * D]
         k[m] = rope_rotate(rms_norm(pk.reshape(-1, H, d), w.k_norm, rms_eps), angles[rows[m]])
         v[m] = pv.reshape(-1, H, d)
@@ -336,7 +347,8 @@ def block_keys_values(x: np.ndarray, weights: List[Weights], seg_off: Sequence[i
 def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
                        angles: np.ndarray, heads: int, rows: Sequence[int], head_dim: int = 128,
                        ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
-                       rounding: Optional[str] = None, kv=None, fp8_in_proj: bool = False) -> dict:
+                       rounding: Optional[str] = None, kv=None, fp8_in_proj: bool = False,
+                       nvfp4_in_proj: bool = False) -> dict:
     """The block's outputs for a few rows, at sizes where the whole block is too slow.
 
     A row's output needs its own q, gate/up and the keys and values of every token it
@@ -351,7 +363,7 @@ def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[
     F = (weights[0].w_in.shape[0] - 3 * D) // 2
     if kv is None:
         kv = block_keys_values(x, weights, seg_off, mod, angles, heads, None, head_dim, ln_eps, rms_eps, stage,
-                               rounding, fp8_in_proj)
+                               rounding, fp8_in_proj, nvfp4_in_proj)
     k, v = kv
     rows = list(rows)
     out = {"k": k, "v": v}
@@ -369,7 +381,7 @@ def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[
         lo, hi = (0, n) if stage == 2 else (seg_off[gkey], seg_off[gkey + 1])
         rr = np.array([rows[i] for i in idx])
         a = _maybe_round(modulate(layer_norm(x[rr], ln_eps), mod[seg[rr], 0], mod[seg[rr], 1]), rounding)
-        p = _in_proj(a, w, fp8_in_proj)
+        p = _in_proj(a, w, _quant(fp8_in_proj, nvfp4_in_proj))
         q = rope_rotate(rms_norm(p[:, 0:D].reshape(-1, H, d), w.q_norm, rms_eps), angles[rr])
         q = _maybe_round(q, rounding)
         o = np.empty((len(rr), H, d))
