@@ -37,14 +37,14 @@ def parse():
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=["joint", "joint_fp8", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
+    p.add_argument("--workload", choices=["joint", "joint_fp8", "joint_nvfp4", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
                                           "loop", "loop_ref"],
                    default="joint",
                    help="joint: the headline 4,256-token joint block.  The others print one line each for "
                         "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
                         "(4096+4096+160 tokens), refs10 / refs10_s1 (image + ten references + text = 45,216 "
-                        "tokens, joint / per-stream block), joint_fp8 (the 4,256-token joint block with the e4m3 input "
-                        "projection), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
+                        "tokens, joint / per-stream block), joint_fp8 / joint_nvfp4 (the 4,256-token joint block with the "
+                        "e4m3 / NVFP4 input projection), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
                         "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager without and with the "
                         "context cache, and as a CUDA graph), loop_ref (the same with one 1024x1024 reference)")
     args = p.parse_args()
@@ -58,7 +58,7 @@ def parse():
 
 # Default (timed steps, warm-up steps) per workload: about half a minute of timed work each
 # (a sampling-loop step is one whole 50-step image, ~3.5 s; ~8 s with a reference).
-DEFAULT_STEPS = {"joint": (1000, 20), "joint_fp8": (1000, 20), "stage1": (1000, 20), "joint_ref": (1000, 20),
+DEFAULT_STEPS = {"joint": (1000, 20), "joint_fp8": (1000, 20), "joint_nvfp4": (1000, 20), "stage1": (1000, 20), "joint_ref": (1000, 20),
                  "refs10": (100, 5), "refs10_s1": (100, 5), "dit": (200, 5), "loop": (2, 1),
                  "loop_ref": (1, 1)}
 
@@ -449,8 +449,8 @@ def run_workload(args):
     stream = torch.cuda.current_stream()
     out = {"impl": "ours", "workload": args.workload, "n_gpus": 1, "data": "synthetic", "dtype": "bf16",
            "higher_is_better": True, "unit": "tokens/s"}
-    if args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1", "joint_fp8"):
-        if args.workload == "joint_fp8":
+    if args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1", "joint_fp8", "joint_nvfp4"):
+        if args.workload in ("joint_fp8", "joint_nvfp4"):
             case = synth.config(1)
         elif args.workload.startswith("refs10"):
             case = synth.config_refs(10, 1 if args.workload == "refs10_s1" else 2, seed=5)
@@ -473,11 +473,16 @@ def run_workload(args):
         w8 = B.Fp8Weights(ws_[0]) if args.workload == "joint_fp8" else None
         if w8 is not None:
             wsp = B.workspace(B.block_fp8_workspace_size(d, N), dev)
+        w4 = B.Nvfp4Weights(ws_[0]) if args.workload == "joint_nvfp4" else None
+        if w4 is not None:
+            wsp = B.workspace(B.block_nvfp4_workspace_size(d, N), dev)
 
         def step():
             B.rope_build(d, pos, out=rope, stream=stream)
             if w8 is not None:
                 B.block_fp8_fwd(d, w8, case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
+            elif w4 is not None:
+                B.block_nvfp4_fwd(d, w4, case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
             elif case.stage == 1:
                 B.stream_block_fwd(d, ws_, case.seg_off, mod, x, rope, x_out=x_out, ws=wsp, stream=stream)
             else:

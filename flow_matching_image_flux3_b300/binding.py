@@ -37,6 +37,11 @@ class flux3_block_weights_fp8(ctypes.Structure):
                 ("b_out", c_vp)]
 
 
+class flux3_block_weights_nvfp4(ctypes.Structure):
+    _fields_ = [("w_in", c_vp), ("w_sf", c_vp), ("s_in", c_vp), ("b_in", c_vp), ("q_norm", c_vp), ("k_norm", c_vp),
+                ("w_out", c_vp), ("b_out", c_vp)]
+
+
 class flux3_segments(ctypes.Structure):
     _fields_ = [("n_seg", c_i32), ("seg_off", ctypes.POINTER(c_i32)), ("mod", c_vp)]
 
@@ -103,6 +108,13 @@ def _load() -> ctypes.CDLL:
                                         c_i32, c_vp, c_vp, c_size, c_vp]),
         "flux3_sample_fwd": (c_i32, [P(flux3_dims), P(flux3_dit_weights), P(flux3_sample_args), c_vp, c_vp, c_size,
                                      c_vp]),
+        "flux3_nvfp4_scale_bytes": (c_size, [c_i32, c_i32]),
+        "flux3_quantize_rows_nvfp4": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
+        "flux3_in_proj_nvfp4_fwd": (c_i32, [P(flux3_dims), P(flux3_block_weights_nvfp4), c_vp, c_vp, c_vp, c_i32, c_vp,
+                                            c_vp, c_vp, c_vp, c_i32, c_vp, c_vp]),
+        "flux3_block_nvfp4_workspace_size": (c_size, [P(flux3_dims), c_i32]),
+        "flux3_block_nvfp4_fwd": (c_i32, [P(flux3_dims), P(flux3_block_weights_nvfp4), P(flux3_segments), c_vp, c_vp,
+                                          c_i32, c_vp, c_vp, c_size, c_vp]),
         "flux3_block_fwd_static": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp,
                                            c_i32, c_vp, c_vp]),
         "flux3_device_error": (c_i32, [P(ctypes.c_uint32), c_i32]),
@@ -125,7 +137,8 @@ EXPORTED = [
     "flux3_device_error", "flux3_profile_begin", "flux3_profile_end", "flux3_block_fwd_static",
     "flux3_sigma_schedule", "flux3_linear_fwd", "flux3_cfg_euler_step", "flux3_sample_workspace_size",
     "flux3_sample_fwd", "flux3_quantize_rows_fp8", "flux3_in_proj_fp8_fwd", "flux3_block_fp8_workspace_size",
-    "flux3_block_fp8_fwd", "flux3_selftest_timeout",
+    "flux3_block_fp8_fwd", "flux3_selftest_timeout", "flux3_nvfp4_scale_bytes", "flux3_quantize_rows_nvfp4",
+    "flux3_in_proj_nvfp4_fwd", "flux3_block_nvfp4_workspace_size", "flux3_block_nvfp4_fwd",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -493,6 +506,80 @@ def block_fp8_fwd(dims, weights: Fp8Weights, seg_off: Sequence[int], mod: torch.
                                                           _ptr(x, torch.bfloat16), _ptr(x_out, torch.bfloat16), n,
                                                           _ptr(rope, torch.float32), _ptr(ws), ws.numel(),
                                                           _stream(stream)))
+    return x_out
+
+
+def nvfp4_scale_bytes(rows: int, k: int) -> int:
+    return int(lib.flux3_nvfp4_scale_bytes(rows, k))
+
+
+def quantize_rows_nvfp4(x: torch.Tensor, stream=None):
+    """NVFP4 codes (uint8 [rows, k / 2], two per byte), tiled block scales (uint8) and fp32
+    row scales [rows] of a bf16 matrix."""
+    rows, k = x.shape
+    q = torch.empty(rows, k // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(max(1, nvfp4_scale_bytes(rows, k)), dtype=torch.uint8, device=x.device)
+    sc = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check("flux3_quantize_rows_nvfp4", lib.flux3_quantize_rows_nvfp4(_ptr(x, torch.bfloat16), rows, k, _ptr(q), _ptr(sf),
+                                                                      _ptr(sc), _stream(stream)))
+    return q, sf, sc
+
+
+class Nvfp4Weights:
+    """A block's weights with the input projection quantized to NVFP4 (on the device,
+    through flux3_quantize_rows_nvfp4); W_out, norms and biases as given."""
+
+    def __init__(self, w, stream=None):
+        self.w_in, self.w_sf, self.s_in = quantize_rows_nvfp4(w.w_in, stream)
+        self.b_in, self.q_norm, self.k_norm = w.b_in, w.q_norm, w.k_norm
+        self.w_out, self.b_out = w.w_out, w.b_out
+
+
+def _nvfp4_struct(w: Nvfp4Weights) -> flux3_block_weights_nvfp4:
+    return flux3_block_weights_nvfp4(_ptr(w.w_in, torch.uint8), _ptr(w.w_sf, torch.uint8), _ptr(w.s_in, torch.float32),
+                                     _ptr(w.b_in, torch.float32), _ptr(w.q_norm, torch.float32),
+                                     _ptr(w.k_norm, torch.float32), _ptr(w.w_out, torch.bfloat16),
+                                     _ptr(w.b_out, torch.float32))
+
+
+def in_proj_nvfp4_fwd(dims, weights: Nvfp4Weights, a4: torch.Tensor, a_sf: torch.Tensor, sa: torch.Tensor,
+                      rope: torch.Tensor, stream=None):
+    """in_proj_fwd (one weight set) on NVFP4 codes a4 (uint8 [N, D / 2]) with tiled block
+    scales a_sf and per-token scales sa (fp32 [N])."""
+    n = a4.shape[0]
+    D, H, F = dims.width, dims.heads, dims.ffn_hidden
+    dev = a4.device
+    q = torch.empty(H, n, 128, dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    ldv = ld_vt(n)
+    vt = torch.zeros(H, 128, ldv, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(n, D + F, dtype=torch.bfloat16, device=dev)
+    d = make_dims(dims)
+    w = _nvfp4_struct(weights)
+    _check("flux3_in_proj_nvfp4_fwd", lib.flux3_in_proj_nvfp4_fwd(
+        ctypes.byref(d), ctypes.byref(w), _ptr(a4, torch.uint8), _ptr(a_sf, torch.uint8), _ptr(sa, torch.float32), n,
+        _ptr(rope, torch.float32), _ptr(q), _ptr(k), _ptr(vt), ldv, _ptr(y), _stream(stream)))
+    return q, k, vt, y
+
+
+def block_nvfp4_workspace_size(dims, n: int) -> int:
+    d = make_dims(dims)
+    return int(lib.flux3_block_nvfp4_workspace_size(ctypes.byref(d), n))
+
+
+def block_nvfp4_fwd(dims, weights: Nvfp4Weights, seg_off: Sequence[int], mod: torch.Tensor, x: torch.Tensor,
+                    rope: torch.Tensor, x_out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """The joint block with the NVFP4 input projection."""
+    n = x.shape[0]
+    x_out = x_out if x_out is not None else torch.empty_like(x)
+    ws = ws if ws is not None else workspace(block_nvfp4_workspace_size(dims, n), x.device)
+    d, s = make_dims(dims), Segments(seg_off, mod)
+    w = _nvfp4_struct(weights)
+    _check("flux3_block_nvfp4_fwd", lib.flux3_block_nvfp4_fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(s.s),
+                                                              _ptr(x, torch.bfloat16), _ptr(x_out, torch.bfloat16), n,
+                                                              _ptr(rope, torch.float32), _ptr(ws), ws.numel(),
+                                                              _stream(stream)))
     return x_out
 
 

@@ -15,6 +15,7 @@
 #include "sm103.cuh"
 #include "simt.cuh"
 #include "gemm.cuh"
+#include "gemm_nvf4.cuh"
 #include "attention.cuh"
 
 using namespace f3;
@@ -206,9 +207,9 @@ flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& 
     return launch_status();
 }
 
-// Clusters of two CTAs that can be resident at once for a GEMM instantiation (SMs are
-// paired within a GPC, so this can be below half the SM count); cached per device.
-template <int BN, int EPI, int AK>
+// Clusters of two CTAs that can be resident at once for a GEMM kernel (SMs are paired
+// within a GPC, so this can be below half the SM count); cached per device.
+template <auto Kernel>
 int max_active_pairs(int smem, int sms) {
     static std::atomic<int> cache[64] = {};  // host threads may launch concurrently
     int dev = 0;
@@ -227,27 +228,21 @@ int max_active_pairs(int smem, int sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<BN, EPI, 2, AK>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, Kernel, &cfg) != cudaSuccess) return 0;
     cache[dev].store(n, std::memory_order_release);
     return n;
 }
 
-template <int BN, int EPI, int CL, int AK = 0>
-flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
-    const int tasks = (P.m_tiles / CL) * P.n_tiles;
+// A persistent GEMM kernel in clusters of two: one cluster per resident pair, at most one
+// per pair of tiles.
+template <auto Kernel>
+flux3_status launch_pairs(const GemmParams& P, int smem, cudaStream_t st, int kind) {
+    const int tasks = (P.m_tiles / 2) * P.n_tiles;
     if (tasks == 0) return FLUX3_OK;
-    const int smem = GemmCfg<BN>::SMEM_BYTES;
-    if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL, AK>>(smem)) return FLUX3_ERR_CUDA;
+    if (!smem_attr_once<Kernel>(smem)) return FLUX3_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return FLUX3_ERR_CUDA;
-    if constexpr (CL == 1) {
-        const int grid = tasks < sms ? tasks : sms;
-        prof_before(kind, st);
-        gemm_tcgen05_kernel<BN, EPI, CL, AK><<<grid, GEMM_THREADS, smem, st>>>(P);
-        prof_after(st);
-        return launch_status();
-    } else {
-    const int pairs = max_active_pairs<BN, EPI, AK>(smem, sms);
+    const int pairs = max_active_pairs<Kernel>(smem, sms);
     if (pairs <= 0) return FLUX3_ERR_CUDA;
     const int units = tasks < pairs ? tasks : pairs;  // persistent: every cluster resident at once
     cudaLaunchConfig_t cfg = {};
@@ -263,9 +258,27 @@ flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     prof_before(kind, st);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<BN, EPI, CL, AK>, P);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, Kernel, P);
     prof_after(st);
     return e == cudaSuccess ? launch_status() : FLUX3_ERR_CUDA;
+}
+
+template <int BN, int EPI, int CL, int AK = 0>
+flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
+    const int smem = GemmCfg<BN>::SMEM_BYTES;
+    if constexpr (CL == 1) {
+        const int tasks = P.m_tiles * P.n_tiles;
+        if (tasks == 0) return FLUX3_OK;
+        if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL, AK>>(smem)) return FLUX3_ERR_CUDA;
+        const int sms = sm_count();
+        if (sms <= 0) return FLUX3_ERR_CUDA;
+        const int grid = tasks < sms ? tasks : sms;
+        prof_before(kind, st);
+        gemm_tcgen05_kernel<BN, EPI, CL, AK><<<grid, GEMM_THREADS, smem, st>>>(P);
+        prof_after(st);
+        return launch_status();
+    } else {
+        return launch_pairs<gemm_tcgen05_kernel<BN, EPI, 2, AK>>(P, smem, st, kind);
     }
 }
 
@@ -343,6 +356,47 @@ flux3_status run_quantize_rows(const void* x, int rows, int k, void* q, float* s
     prof_before(FLUX3_KERNEL_QUANTIZE, st);
     quantize_rows_e4m3_kernel<<<(rows + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, k,
                                                              static_cast<uint8_t*>(q), scale);
+    prof_after(st);
+    return launch_status();
+}
+
+// the input projection on NVFP4 operands (one weight set): a4 [N, D / 2] codes, a_sf the
+// tiled block scales, sa the per-token scales
+flux3_status run_in_proj_nvfp4(const flux3_dims* d, const flux3_block_weights_nvfp4* w, const void* a4, const void* a_sf,
+                               const float* sa, int N, const float* rope, void* q, void* k, void* vt, int ld_vt, void* y,
+                               cudaStream_t st) {
+    if (N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    const int D = d->width, F = d->ffn_hidden, H = d->heads;
+    const int n_in = 3 * D + 2 * F;
+    if (!tmap_2d_u8(&P.tm_a, a4, D / 2, N, (uint64_t)D / 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_2d_u8(&P.tm_b[0], w->w_in, D / 2, n_in, (uint64_t)D / 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    P.ew[0] = {w->b_in, w->q_norm, w->k_norm, w->s_in, static_cast<const uint8_t*>(w->w_sf)};
+    const int32_t one[2] = {0, N};
+    fill_groups(P, one, 1, 1, N, 2);
+    P.n_tiles = 3 * H / 2 + F / 128;
+    P.k_blocks = D / 256;
+    P.sf_steps = D / 64;
+    P.a_scale = sa;
+    P.a_sf = static_cast<const uint8_t*>(a_sf);
+    P.heads = H; P.width = D; P.ffn = F; P.n_tokens = N; P.ld_vt = ld_vt; P.ld_y = D + F;
+    P.rms_eps = d->rms_eps;
+    P.rope = rope;
+    P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
+    P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
+    return launch_pairs<gemm_nvf4_kernel<2>>(P, Nvf4Cfg::SMEM_BYTES, st, FLUX3_KERNEL_IN_PROJ);
+}
+
+// rows padded to a pair of 128-row tiles: the scale rows an NVFP4 GEMM may read
+int nvfp4_rows_padded(int rows) { return (rows + 255) / 256 * 256; }
+
+flux3_status run_quantize_rows_nvfp4(const void* x, int rows, int k, void* q, void* sf, float* scale, cudaStream_t st) {
+    if (rows == 0) return FLUX3_OK;
+    const int rp = nvfp4_rows_padded(rows);
+    prof_before(FLUX3_KERNEL_QUANTIZE, st);
+    quantize_rows_nvfp4_kernel<<<rp / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, rp, k,
+                                                       static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf), scale);
     prof_after(st);
     return launch_status();
 }
@@ -1020,6 +1074,99 @@ flux3_status flux3_block_fp8_fwd(const flux3_dims* dims, const flux3_block_weigh
     if ((s = run_adaln(dims, segs->mod, seg_table(segs->seg_off, segs->n_seg), x, N, b.a, st)) != FLUX3_OK) return s;
     if ((s = run_quantize_rows(b.a, N, D, a8, sa, st)) != FLUX3_OK) return s;
     if ((s = run_in_proj_fp8(dims, w, 1, segs, a8, sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK) return s;
+    const int32_t full[2] = {0, N};
+    if ((s = run_attn(dims, b.q, b.k, b.vt, b.ld_vt, N, full, 1, b.y, D + F, false, st)) != FLUX3_OK) return s;
+    const flux3_block_weights wo{nullptr, nullptr, nullptr, nullptr, w->w_out, w->b_out};
+    return run_out_proj(dims, &wo, 1, segs, b.y, x, x_out, N, st);
+}
+
+size_t flux3_nvfp4_scale_bytes(int32_t rows, int32_t k) {
+    if (rows < 0 || rows > kMaxTokens * 16 || k <= 0 || k > (1 << 20) || k % 64 != 0) return 0;
+    return (size_t)nvfp4_rows_padded(rows) * (size_t)(k / 16);
+}
+
+flux3_status flux3_quantize_rows_nvfp4(const void* x, int32_t rows, int32_t k, void* q, void* sf, float* scale,
+                                       flux3_stream_t stream) {
+    if (rows < 0 || rows > kMaxTokens * 16 || k <= 0 || k > (1 << 20)) return FLUX3_ERR_INVALID_ARG;
+    if (k % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (rows == 0) return FLUX3_OK;
+    if (!x || !q || !sf || !scale || !al16(x) || !al16(q) || !al16(sf)) return FLUX3_ERR_INVALID_ARG;
+    return run_quantize_rows_nvfp4(x, rows, k, q, sf, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static flux3_status check_weights_nvfp4(const flux3_block_weights_nvfp4* w) {
+    if (!w || !w->w_in || !al16(w->w_in) || !w->w_sf || !al16(w->w_sf) || !w->s_in || !w->q_norm || !al16(w->q_norm) ||
+        !w->k_norm || !al16(w->k_norm) || (w->b_in && !al16(w->b_in)))
+        return FLUX3_ERR_INVALID_ARG;
+    return FLUX3_OK;
+}
+
+flux3_status flux3_in_proj_nvfp4_fwd(const flux3_dims* dims, const flux3_block_weights_nvfp4* w, const void* a4,
+                                     const void* a_sf, const float* sa, int32_t n_tokens, const float* rope, void* q,
+                                     void* k, void* vt, int32_t ld_vt, void* y, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (dims->width % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_weights_nvfp4(w)) != FLUX3_OK) return s;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!a4 || !a_sf || !sa || !rope || !q || !k || !vt || !y) return FLUX3_ERR_INVALID_ARG;
+    if (!al16(a4) || !al16(a_sf) || !al16(rope) || !al16(q) || !al16(k) || !al16(vt) || !al16(y)) return FLUX3_ERR_INVALID_ARG;
+    if (ld_vt < n_tokens || ld_vt % 8 != 0) return FLUX3_ERR_INVALID_ARG;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    return run_in_proj_nvfp4(dims, w, a4, a_sf, sa, n_tokens, rope, q, k, vt, ld_vt, y,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+struct Nvfp4Ws {
+    uint8_t *a4, *sf;
+    float* sa;
+    size_t bytes;
+};
+Nvfp4Ws block_nvfp4_ws(const flux3_dims* d, int N, uint8_t* base) {
+    const BlockWs b = block_ws_layout(d, N, nullptr);
+    Nvfp4Ws w;
+    size_t off = b.bytes;
+    w.a4 = base ? base + off : nullptr;
+    off += up256((size_t)N * d->width / 2);
+    w.sf = base ? base + off : nullptr;
+    off += up256((size_t)nvfp4_rows_padded(N) * (d->width / 16));
+    w.sa = base ? reinterpret_cast<float*>(base + off) : nullptr;
+    off += up256((size_t)N * 4);
+    w.bytes = off;
+    return w;
+}
+}  // namespace
+
+size_t flux3_block_nvfp4_workspace_size(const flux3_dims* dims, int32_t n_tokens) {
+    if (check_dims(dims) != FLUX3_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
+    return block_nvfp4_ws(dims, n_tokens, nullptr).bytes;
+}
+
+flux3_status flux3_block_nvfp4_fwd(const flux3_dims* dims, const flux3_block_weights_nvfp4* w, const flux3_segments* segs,
+                                   const void* x, void* x_out, int32_t n_tokens, const float* rope, void* ws,
+                                   size_t ws_bytes, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (dims->width % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    const int N = n_tokens;
+    if (N < 0 || N > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, N, true)) != FLUX3_OK) return s;
+    if ((s = check_weights_nvfp4(w)) != FLUX3_OK) return s;
+    if (!w->w_out || !al16(w->w_out) || (w->b_out && !al16(w->b_out))) return FLUX3_ERR_INVALID_ARG;
+    if (N == 0) return FLUX3_OK;
+    if (!x || !x_out || !rope || !al16(x) || !al16(x_out) || !al16(rope)) return FLUX3_ERR_INVALID_ARG;
+    if (!ws || !al256(ws) || ws_bytes < flux3_block_nvfp4_workspace_size(dims, N)) return FLUX3_ERR_WORKSPACE;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const BlockWs b = block_ws_layout(dims, N, static_cast<uint8_t*>(ws));
+    const Nvfp4Ws nw = block_nvfp4_ws(dims, N, static_cast<uint8_t*>(ws));
+    const int D = dims->width, F = dims->ffn_hidden;
+    if ((s = run_adaln(dims, segs->mod, seg_table(segs->seg_off, segs->n_seg), x, N, b.a, st)) != FLUX3_OK) return s;
+    if ((s = run_quantize_rows_nvfp4(b.a, N, D, nw.a4, nw.sf, nw.sa, st)) != FLUX3_OK) return s;
+    if ((s = run_in_proj_nvfp4(dims, w, nw.a4, nw.sf, nw.sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK)
+        return s;
     const int32_t full[2] = {0, N};
     if ((s = run_attn(dims, b.q, b.k, b.vt, b.ld_vt, N, full, 1, b.y, D + F, false, st)) != FLUX3_OK) return s;
     const flux3_block_weights wo{nullptr, nullptr, nullptr, nullptr, w->w_out, w->b_out};

@@ -31,7 +31,8 @@ struct EpiWeights {
     const float* bias;
     const float* q_norm;
     const float* k_norm;
-    const float* w_scale;  // e4m3 operands: scale of each weight row (output column)
+    const float* w_scale;  // e4m3 / NVFP4 operands: scale of each weight row (output column)
+    const uint8_t* w_sf;   // NVFP4 operands: the weight's tiled block scales
 };
 
 struct GemmParams {
@@ -41,7 +42,9 @@ struct GemmParams {
     GemmGroup grp[FLUX3_MAX_SEGMENTS];
     int n_groups;
     int m_tiles, n_tiles, k_blocks;
-    const float* a_scale;  // e4m3 operands: scale of each A row (token)
+    const float* a_scale;  // e4m3 / NVFP4 operands: scale of each A row (token)
+    const uint8_t* a_sf;   // NVFP4 operands: A's tiled block scales
+    int sf_steps;          // NVFP4: 64-element steps per row (K / 64)
     // EPI_QKV_SWIGLU
     int heads, width, ffn, n_tokens, ld_vt, ld_y;
     float rms_eps;
@@ -105,8 +108,8 @@ F3_DEV void unpack32(const uint32_t (&r)[32], float* v) {
 }
 
 // --------------------------------------------------------------------- epilogues
-// AK = 1: the operands were e4m3 codes; the accumulator is scaled by the token's and the
-// weight row's scales before the epilogue proper.
+// AK = 1 (e4m3 codes) or 2 (NVFP4 codes, block scales already applied by the MMA): the
+// accumulator is scaled by the token's and the weight row's scales before the epilogue proper.
 template <int AK>
 F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
     const int nq = 3 * p.heads / 2;

@@ -249,6 +249,84 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bflo
     }
 }
 
+// ---------------------------------------------------------------- NVFP4 row quantization
+// One warp per row ("FLUX.3" cookbook, section 3: FP4 (E2M1) values with FP8 block scales):
+//   g = 2688 / amax (2688 = 6 x 448; g overflowing fp32 counts as a zero row), s_row = amax / 2688
+//   per 16 elements: sb = e4m3(bmax * g / 6), codes = e2m1(x * (g / sb)) (0 where sb = 0)
+// every step one fp32 operation rounded to nearest even, e4m3 and E2M1 saturating.
+// Codes: two per byte, even element in the low nibble.  Block scales: the tiled layout
+// the block-scaled MMA reads (512 bytes per 128 rows x 64 elements, row r's four scales
+// of a 64-element step at byte (r % 32) * 16 + ((r % 128) / 32) * 4), rows from `rows` up
+// to rows_padded written as zero scales.  k % 256 == 0.
+__global__ void __launch_bounds__(256) quantize_rows_nvfp4_kernel(const __nv_bfloat16* __restrict__ x, int rows,
+                                                                 int rows_padded, int k, uint8_t* __restrict__ q,
+                                                                 uint8_t* __restrict__ sf, float* __restrict__ scale) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= rows_padded) return;
+    const int groups = k / 64;
+    // this row's 4-byte slot in the tile of 64-element step 0; step g is g * 512 bytes on
+    uint32_t* sfr = reinterpret_cast<uint32_t*>(sf + (size_t)(r / 128) * groups * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4);
+    if (r >= rows) {
+        for (int g = lane; g < groups; g += 32) sfr[(size_t)g * 128] = 0u;
+        return;
+    }
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * k);
+    float amax = 0.f;
+    for (int c = lane; c < k / 8; c += 32) {
+        const uint4 u = __ldg(xr + c);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float g = amax > 0.f ? __fdiv_rn(2688.f, amax) : 0.f;
+    if (!(g <= 3.402823466e38f)) g = 0.f;
+    if (lane == 0) scale[r] = g > 0.f ? __fdiv_rn(amax, 2688.f) : 0.f;
+    uint4* qr = reinterpret_cast<uint4*>(q + (size_t)r * (k / 2));
+    for (int grp = lane; grp < groups; grp += 32) {
+        uint32_t sbw = 0;
+        uint32_t codes[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint4 u0 = __ldg(xr + grp * 8 + 2 * b), u1 = __ldg(xr + grp * 8 + 2 * b + 1);
+            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[2 * e] = __uint_as_float(w[e] << 16);
+                v[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
+            float bmax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+            const float u = __fdiv_rn(__fmul_rn(bmax, g), 6.f);
+            uint16_t h;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.f), "f"(u));  // low byte = u
+            const uint32_t c = h & 0xFFu, ce = c >> 3, cm = c & 7u;
+            const float sbf = ce ? __uint_as_float(((ce + 120u) << 23) | (cm << 20)) : (float)cm * 0.001953125f;
+            const float rr = sbf > 0.f ? __fdiv_rn(g, sbf) : 0.f;
+            sbw |= c << (8 * b);
+            codes[2 * b] = codes[2 * b + 1] = 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float a0 = sbf > 0.f ? __fmul_rn(v[2 * j], rr) : 0.f;
+                const float a1 = sbf > 0.f ? __fmul_rn(v[2 * j + 1], rr) : 0.f;
+                uint32_t byte;
+                asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+                    : "=r"(byte)
+                    : "f"(a1), "f"(a0));  // low nibble = the even element
+                codes[2 * b + j / 4] |= byte << (8 * (j % 4));
+            }
+        }
+        qr[grp * 2] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        qr[grp * 2 + 1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        sfr[(size_t)grp * 128] = sbw;
+    }
+}
+
 // ---------------------------------------------------------------- guided Euler update
 // latent += dt * (v_neg + s (v_pos - v_neg)) (v_neg == nullptr: latent += dt * v_pos); the
 // updated latent rounded to bf16 goes to lat_bf (the next step's embedder input) if given.

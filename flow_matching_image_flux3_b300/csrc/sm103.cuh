@@ -257,6 +257,41 @@ F3_DEV void mma_commit_multicast_if(bool issue, uint32_t bar, uint16_t cta_mask)
         : "memory");
 }
 
+// D[tmem] (+)= (A * sfA)[smem] (B * sfB)[smem]^T on E2M1 operands (two per byte, K-major,
+// K = 64 per instruction = 32 bytes of each row) with one e4m3 scale per 16 elements of
+// K (kind::mxf4nvf4, scale_vec::4X).  sfa / sfb are the TMEM addresses of the scales:
+// 4 columns for 128 rows of A, 8 for 256 rows of B (the tmem_cp_32x128b_x4 layout).
+F3_DEV void mma_nvf4_ss_if(bool issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                           uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 q, %7, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate), "r"((uint32_t)issue)
+        : "memory");
+}
+// TMEM <- shared: 32 rows of 16 bytes (no swizzle, 8-row groups 128 bytes apart), row i to
+// lane i of each of the four 32-lane quarters, bytes 4c..4c+3 to column taddr + c.
+F3_DEV void tmem_cp_32x128b_x4_if(bool issue, uint32_t taddr, uint32_t saddr) {
+    const uint64_t desc = (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) |
+                          ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %2, 0;\n\t"
+        "@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(desc), "r"((uint32_t)issue)
+        : "memory");
+}
+// 1-D bulk copy global -> this CTA's shared memory (both 16-byte aligned, bytes % 16 == 0),
+// counted on the mbarrier's transaction bytes.
+F3_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32*(w%4)..).
 F3_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -322,6 +357,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
     return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4nvf4: A = B = E2M1 (format code 1), scales UE4M3
+// (bit 23 clear), scale data ids 0 (all four bytes of a scale column), D = fp32, K-major.
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ small helpers

@@ -315,7 +315,7 @@ flux3_status flux3_sample_fwd(const flux3_dims *dims, const flux3_dit_weights *w
  * then the same epilogues as flux3_in_proj_fwd.  The output projection stays bf16.
  * Quantization (flux3_quantize_rows_fp8) is per row: scale = amax / 448, codes =
  * e4m3(x * (448 / amax)) rounded to nearest even, saturated at +-448, all in fp32
- * (an all-zero row: zero codes, scale 0).  NVFP4 (block-scaled) is not provided. */
+ * (an all-zero row: zero codes, scale 0).  NVFP4: below. */
 
 /* Row-wise e4m3 quantization of a bf16 [rows, k] matrix, k % 256 == 0.
  * q      device uint8 [rows, k]: e4m3 codes;  scale  device fp32 [rows]. */
@@ -353,6 +353,65 @@ size_t flux3_block_fp8_workspace_size(const flux3_dims *dims, int32_t n_tokens);
 flux3_status flux3_block_fp8_fwd(const flux3_dims *dims, const flux3_block_weights_fp8 *w, const flux3_segments *segs,
                                  const void *x, void *x_out, int32_t n_tokens, const float *rope, void *ws,
                                  size_t ws_bytes, flux3_stream_t stream);
+
+/* ---- NVFP4 input projection.  The cookbook's NVFP4 checkpoints store FP4 (E2M1) values
+ * with FP8 block scales and need a Blackwell GEMM (SGLang cookbook FLUX.3, section 3,
+ * Quantized checkpoints).  Here both operands of the input projection are NVFP4 and the
+ * product runs on the block-scaled tensor cores (tcgen05 kind::mxf4nvf4):
+ *   P = s_a[token] * sum_k (e2m1(a) sb_a)(e2m1(w) sb_w) * s_w[out] + b_in,
+ * then the same epilogues as flux3_in_proj_fwd; the output projection stays bf16.
+ * Format, per row of a bf16 [rows, k] matrix (k % 256 == 0), every step one fp32 operation
+ * rounded to nearest even:
+ *   g = 2688 / amax (2688 = 6 x 448; an all-zero row, or one whose g overflows fp32,
+ *   gives zero codes and scales), s_row = amax / 2688;
+ *   per 16 consecutive elements: sb = e4m3(bmax * g / 6) (saturating), the codes
+ *   e2m1(x * (g / sb)) (saturating at 6, the sign kept at zero; 0 where sb = 0).
+ * Storage: codes two per byte, the even element in the low nibble ([rows, k / 2] bytes);
+ * block scales in the tiled layout the MMA reads: 512 bytes per 128 rows x 64 elements,
+ * row r's four scales of 64-element step j at byte
+ *   ((r / 128) * (k / 64) + j) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4,
+ * rows padded to a multiple of 256 with zero scales (flux3_nvfp4_scale_bytes). */
+
+/* Bytes of the tiled block scales of a [rows, k] matrix (0 for invalid sizes). */
+size_t flux3_nvfp4_scale_bytes(int32_t rows, int32_t k);
+
+/* NVFP4 quantization of a bf16 [rows, k] matrix (device), k % 256 == 0.
+ * q  uint8 [rows, k / 2] codes;  sf  uint8 [flux3_nvfp4_scale_bytes(rows, k)] block scales;
+ * scale  fp32 [rows].  All 16-byte aligned except scale. */
+flux3_status flux3_quantize_rows_nvfp4(const void *x, int32_t rows, int32_t k, void *q, void *sf, float *scale,
+                                       flux3_stream_t stream);
+
+/* One block's parameters with an NVFP4 input projection (device memory).
+ *  w_in  uint8 [3D + 2F, D / 2]: W_in codes (rows Q | K | V | gate | up), w_sf their tiled
+ *        block scales, s_in fp32 [3D + 2F] their row scales (flux3_quantize_rows_nvfp4).
+ *  Other fields as flux3_block_weights. */
+typedef struct flux3_block_weights_nvfp4 {
+    const void *w_in;
+    const void *w_sf;
+    const float *s_in;
+    const float *b_in;
+    const float *q_norm;
+    const float *k_norm;
+    const void *w_out;
+    const float *b_out;
+} flux3_block_weights_nvfp4;
+
+/* flux3_in_proj_fwd (one weight set) on NVFP4 operands: a4 uint8 [N, D / 2] codes of the
+ * modulated input, a_sf their tiled block scales, sa fp32 [N] their row scales.  D % 256 == 0.
+ * Outputs and other arguments as flux3_in_proj_fwd. */
+flux3_status flux3_in_proj_nvfp4_fwd(const flux3_dims *dims, const flux3_block_weights_nvfp4 *w, const void *a4,
+                                     const void *a_sf, const float *sa, int32_t n_tokens, const float *rope, void *q,
+                                     void *k, void *vt, int32_t ld_vt, void *y, flux3_stream_t stream);
+
+size_t flux3_block_nvfp4_workspace_size(const flux3_dims *dims, int32_t n_tokens);
+
+/* The joint block (stage 2) with the NVFP4 input projection: LayerNorm + modulation (bf16),
+ * NVFP4 row quantization, the block-scaled input projection with its epilogues, attention,
+ * bf16 output projection with the gated residual.  Arguments as flux3_block_fwd; workspace
+ * flux3_block_nvfp4_workspace_size bytes. */
+flux3_status flux3_block_nvfp4_fwd(const flux3_dims *dims, const flux3_block_weights_nvfp4 *w,
+                                   const flux3_segments *segs, const void *x, void *x_out, int32_t n_tokens,
+                                   const float *rope, void *ws, size_t ws_bytes, flux3_stream_t stream);
 
 /* ---- flux3_block_fwd without a caller-provided workspace.
  * This entry point has no counterpart in the model description; it is a service for

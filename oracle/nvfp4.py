@@ -19,15 +19,15 @@ Readings where the pages are silent (listed in the design notes with the rest):
         per block: sb = e4m3(fp32(fp32(bmax * g) / 6))              bmax = max |x| in block
         per element: code = e2m1(fp32(x * fp32(g / sb)))            (code 0 where sb = 0)
     each rounding to nearest even, e4m3 and E2M1 saturating (at 448 and 6); the sign of
-    an element that rounds to zero is kept (code 8 is -0); an all-zero row quantizes to
-    zeros with s_row = 0;
+    an element that rounds to zero is kept (code 8 is -0); an all-zero row, and a row so
+    small that g overflows fp32, quantizes to zeros with s_row = 0;
   - then x ~ e2m1(code) * e4m3(sb) * s_row and
         P = s_a[token] * sum_k (e2m1(a) sb_a)(e2m1(w) sb_w) * s_w[out] + b_in.
 Storage (a contract between the quantizer and the GEMM, not arithmetic): two codes per
 byte, the even element in the low nibble; the block scales of 128 rows x 64 elements
 (4 scales per row) form one 512-byte tile, row r's scale j at byte
 (r % 32) * 16 + (r // 32) * 4 + j, tiles ordered by row tile, then by 64-element step,
-rows padded to a multiple of 128 with zero scales.
+rows padded to a multiple of 256 (a pair of 128-row tiles) with zero scales.
 
 Pins (tests/test_oracle_nvfp4.py): E2M1 values from the bit-field formula; the rounding
 against a brute-force nearest search with ties to the even code; the quantizer's zero row,
@@ -110,9 +110,11 @@ def quantize_rows(x):
     x32 = np.asarray(x, dtype=F32)
     rows, k = x32.shape
     amax = np.max(np.abs(x32), axis=1)
-    pos = amax > 0
-    safe = np.where(pos, amax, F32(1))
-    g = np.where(pos, F32(ROW_TARGET) / safe, F32(0)).astype(F32)
+    safe = np.where(amax > 0, amax, F32(1))
+    with np.errstate(over="ignore"):
+        g_raw = (F32(ROW_TARGET) / safe).astype(F32)
+    pos = (amax > 0) & np.isfinite(g_raw)
+    g = np.where(pos, g_raw, F32(0)).astype(F32)
     s_row = np.where(pos, safe / F32(ROW_TARGET), F32(0)).astype(F32)
     blocks = x32.reshape(rows, k // BLOCK, BLOCK)
     bmax = np.max(np.abs(blocks), axis=2)
@@ -172,7 +174,7 @@ def scale_tile_offset(r, j, k: int) -> np.ndarray:
 
 
 def scale_bytes(rows: int, k: int) -> int:
-    return (rows + 127) // 128 * 128 * (k // BLOCK)
+    return (rows + 255) // 256 * 256 * (k // BLOCK)
 
 
 def tile_scales(sb, rows_padded: int = None) -> np.ndarray:

@@ -155,3 +155,21 @@ def test_final_and_euler_argument_checks(B):
         == B.ERR_WORKSPACE
     assert B.lib.flux3_euler_step(None, None, 10, 1.0, 0.5, None) == B.ERR_INVALID_ARG
     assert B.lib.flux3_euler_step(None, None, 0, 1.0, 0.5, None) == B.OK
+
+
+def test_nvfp4_argument_checks(B):
+    FAKE16 = 1 << 20
+    assert B.lib.flux3_nvfp4_scale_bytes(300, 3072) == 512 * 192      # rows padded to 256
+    assert B.lib.flux3_nvfp4_scale_bytes(256, 3072) == 256 * 192
+    assert B.lib.flux3_nvfp4_scale_bytes(1, 100) == 0                 # k % 64 != 0
+    assert B.lib.flux3_quantize_rows_nvfp4(FAKE16, 4, 320, FAKE16, FAKE16, FAKE16, None) == B.ERR_UNSUPPORTED
+    assert B.lib.flux3_quantize_rows_nvfp4(FAKE16 + 8, 4, 256, FAKE16, FAKE16, FAKE16, None) == B.ERR_INVALID_ARG
+    assert B.lib.flux3_quantize_rows_nvfp4(None, 0, 256, None, None, None, None) == B.OK
+    d = _dims(B)
+    assert B.lib.flux3_in_proj_nvfp4_fwd(ctypes.byref(d), None, None, None, None, 4, None, None, None, None, 8, None,
+                                         None) == B.ERR_INVALID_ARG     # no weights
+    w = B.flux3_block_weights_nvfp4(FAKE16, FAKE16, FAKE16, None, FAKE16, FAKE16, FAKE16, None)
+    assert B.lib.flux3_in_proj_nvfp4_fwd(ctypes.byref(d), ctypes.byref(w), FAKE16, FAKE16, FAKE16, 100, FAKE16,
+                                         FAKE16, FAKE16, FAKE16, 96, FAKE16, None) == B.ERR_INVALID_ARG   # ld_vt < N
+    assert B.lib.flux3_block_nvfp4_workspace_size(ctypes.byref(d), 144) > B.lib.flux3_block_workspace_size(
+        ctypes.byref(d), 144)

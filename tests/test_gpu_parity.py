@@ -9,6 +9,7 @@ import torch
 
 import oracle as O
 from oracle import fp8 as Q8
+from oracle import nvfp4 as Q4
 from flow_matching_image_flux3_b300 import synth
 from tests.common import (REL_L2, MAX_ABS, REL_L2_F32, assert_close, rel_l2, max_abs, f64, DevWeights,
                           oracle_weights, oracle_block)
@@ -70,14 +71,17 @@ def test_adaln(n, seg, dims):
 
 
 # ------------------------------------------------------------------ a4..a7 input projection
-def _in_proj_oracle(a, weights, seg_off, pos, dims, stage, fp8=False):
+def _in_proj_oracle(a, weights, seg_off, pos, dims, stage, fp8=False, nvfp4=False):
     D, H, F = dims.width, dims.heads, dims.ffn_hidden
     n = a.shape[0]
     ang = O.rope_angles(pos, dims.rope_theta)
     q = np.empty((n, H, 128)); k = np.empty((n, H, 128)); v = np.empty((n, H, 128)); act = np.empty((n, F))
     ranges = [(0, n, weights[0])] if stage == 2 else [(seg_off[s], seg_off[s + 1], weights[s]) for s in range(len(seg_off) - 1)]
     for lo, hi, w in ranges:
-        p = (Q8.fp8_linear(a[lo:hi], w.w_in) if fp8 else a[lo:hi] @ w.w_in.T) + w.b_in
+        if nvfp4:
+            p = Q4.nvfp4_linear(a[lo:hi], w.w_in) + w.b_in
+        else:
+            p = (Q8.fp8_linear(a[lo:hi], w.w_in) if fp8 else a[lo:hi] @ w.w_in.T) + w.b_in
         q[lo:hi] = O.rope_rotate(O.rms_norm(p[:, :D].reshape(-1, H, 128), w.q_norm, dims.rms_eps), ang[lo:hi])
         k[lo:hi] = O.rope_rotate(O.rms_norm(p[:, D:2 * D].reshape(-1, H, 128), w.k_norm, dims.rms_eps), ang[lo:hi])
         v[lo:hi] = p[:, 2 * D:3 * D].reshape(-1, H, 128)

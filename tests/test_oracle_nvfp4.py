@@ -54,10 +54,12 @@ def _rng(seed):
 
 
 def test_zero_row_and_zero_block():
-    x = np.zeros((2, 64), dtype=F32)
+    x = np.zeros((3, 64), dtype=F32)
     x[1, 16:32] = _rng(1).standard_normal(16)
+    x[2, 5] = F32(1e-40)                 # a subnormal row maximum: 2688 / amax overflows fp32
     codes, sb, s = Q.quantize_rows(x)
     assert (codes[0] == 0).all() and (sb[0] == 0).all() and s[0] == 0
+    assert (codes[2] == 0).all() and (sb[2] == 0).all() and s[2] == 0
     assert (codes[1, :16] == 0).all() and (codes[1, 32:] == 0).all() and sb[1, 0] == 0 and sb[1, 1] > 0
 
 
@@ -115,7 +117,7 @@ def test_storage_layout_inverse_and_packing():
     rng = _rng(7)
     sb = rng.integers(0, 127, size=(200, 768 // 16)).astype(np.uint8)
     buf = Q.tile_scales(sb)
-    assert buf.size == 256 * 48
+    assert buf.size == 256 * 48          # rows padded to a pair of 128-row tiles
     assert (Q.untile_scales(buf, 200, 768) == sb).all()
     assert (buf.reshape(-1)[np.setdiff1d(np.arange(buf.size), Q.scale_tile_offset(*np.meshgrid(
         np.arange(200), np.arange(48), indexing="ij"), 768).ravel())] == 0).all()   # padding rows are zero
