@@ -210,7 +210,7 @@ flux3_status run_adaln(const flux3_dims* d, const float* mod, const SegOffsets& 
 // Clusters of two CTAs that can be resident at once for a GEMM kernel (SMs are paired
 // within a GPC, so this can be below half the SM count); cached per device.
 template <auto Kernel>
-int max_active_pairs(int smem, int sms) {
+int max_active_pairs(int smem, int threads, int sms) {
     static std::atomic<int> cache[64] = {};  // host threads may launch concurrently
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
@@ -218,7 +218,7 @@ int max_active_pairs(int smem, int sms) {
     if (known > 0) return known;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(sms & ~1));
-    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -236,18 +236,18 @@ int max_active_pairs(int smem, int sms) {
 // A persistent GEMM kernel in clusters of two: one cluster per resident pair, at most one
 // per pair of tiles.
 template <auto Kernel>
-flux3_status launch_pairs(const GemmParams& P, int smem, cudaStream_t st, int kind) {
+flux3_status launch_pairs(const GemmParams& P, int smem, int threads, cudaStream_t st, int kind) {
     const int tasks = (P.m_tiles / 2) * P.n_tiles;
     if (tasks == 0) return FLUX3_OK;
     if (!smem_attr_once<Kernel>(smem)) return FLUX3_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return FLUX3_ERR_CUDA;
-    const int pairs = max_active_pairs<Kernel>(smem, sms);
+    const int pairs = max_active_pairs<Kernel>(smem, threads, sms);
     if (pairs <= 0) return FLUX3_ERR_CUDA;
     const int units = tasks < pairs ? tasks : pairs;  // persistent: every cluster resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * units));
-    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -263,22 +263,22 @@ flux3_status launch_pairs(const GemmParams& P, int smem, cudaStream_t st, int ki
     return e == cudaSuccess ? launch_status() : FLUX3_ERR_CUDA;
 }
 
-template <int BN, int EPI, int CL, int AK = 0>
+template <int BN, int EPI, int CL, int AK = 0, int EW = 4>
 flux3_status launch_gemm(const GemmParams& P, cudaStream_t st, int kind) {
     const int smem = GemmCfg<BN>::SMEM_BYTES;
     if constexpr (CL == 1) {
         const int tasks = P.m_tiles * P.n_tiles;
         if (tasks == 0) return FLUX3_OK;
-        if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL, AK>>(smem)) return FLUX3_ERR_CUDA;
+        if (!smem_attr_once<gemm_tcgen05_kernel<BN, EPI, CL, AK, EW>>(smem)) return FLUX3_ERR_CUDA;
         const int sms = sm_count();
         if (sms <= 0) return FLUX3_ERR_CUDA;
         const int grid = tasks < sms ? tasks : sms;
         prof_before(kind, st);
-        gemm_tcgen05_kernel<BN, EPI, CL, AK><<<grid, GEMM_THREADS, smem, st>>>(P);
+        gemm_tcgen05_kernel<BN, EPI, CL, AK, EW><<<grid, gemm_threads(EW), smem, st>>>(P);
         prof_after(st);
         return launch_status();
     } else {
-        return launch_pairs<gemm_tcgen05_kernel<BN, EPI, 2, AK>>(P, smem, st, kind);
+        return launch_pairs<gemm_tcgen05_kernel<BN, EPI, 2, AK, EW>>(P, smem, gemm_threads(EW), st, kind);
     }
 }
 
@@ -348,7 +348,7 @@ flux3_status run_in_proj_fp8(const flux3_dims* d, const flux3_block_weights_fp8*
     P.rope = rope;
     P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
     P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
-    return launch_gemm<256, EPI_QKV_SWIGLU, 2, 1>(P, st, FLUX3_KERNEL_IN_PROJ);
+    return launch_gemm<256, EPI_QKV_SWIGLU, 2, 1, 8>(P, st, FLUX3_KERNEL_IN_PROJ);
 }
 
 flux3_status run_quantize_rows(const void* x, int rows, int k, void* q, float* scale, cudaStream_t st) {
@@ -385,7 +385,7 @@ flux3_status run_in_proj_nvfp4(const flux3_dims* d, const flux3_block_weights_nv
     P.rope = rope;
     P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
     P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
-    return launch_pairs<gemm_nvf4_kernel<2>>(P, Nvf4Cfg::SMEM_BYTES, st, FLUX3_KERNEL_IN_PROJ);
+    return launch_pairs<gemm_nvf4_kernel<2, 8>>(P, Nvf4Cfg::SMEM_BYTES, gemm_threads(8), st, FLUX3_KERNEL_IN_PROJ);
 }
 
 // rows padded to a pair of 128-row tiles: the scale rows an NVFP4 GEMM may read

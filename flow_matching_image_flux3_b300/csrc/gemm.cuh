@@ -7,9 +7,10 @@
 //   EPI_F32             plain fp32 store (+ bias): the output layer
 //   EPI_BF16            plain bf16 store (+ bias): the token embedders
 //
-// Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads, warp 1 issues
-// tcgen05.mma and owns the TMEM allocation (both run as converged warps with one elected
-// lane issuing), warps 2..5 run the epilogue, one accumulator row (TMEM lane) per thread.
+// Warp roles (one CTA per SM): warp 0 issues TMA loads, warp 1 issues tcgen05.mma and
+// owns the TMEM allocation (both run as converged warps with one elected lane issuing),
+// warps 2.. run the epilogue, one accumulator row (TMEM lane) per thread: 4 warps, or 8
+// (two per TMEM lane quarter, each taking half of a tile's columns).
 // Two TMEM accumulators let the epilogue of one tile overlap the MMAs of the next.
 #pragma once
 #include <cuda.h>
@@ -20,7 +21,9 @@ namespace f3 {
 
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;  // bf16 elements per 128-byte swizzle row
-constexpr int GEMM_THREADS = 192;
+// Threads of a GEMM CTA with `ew` epilogue warps (4, or 8 for the quantized input
+// projections, whose shorter mainloop no longer hides a 4-warp epilogue).
+__host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 
 enum EpiKind { EPI_QKV_SWIGLU = 0, EPI_GATED_RESIDUAL = 1, EPI_F32 = 2, EPI_BF16 = 3 };
 
@@ -108,73 +111,99 @@ F3_DEV void unpack32(const uint32_t (&r)[32], float* v) {
 }
 
 // --------------------------------------------------------------------- epilogues
-// AK = 1 (e4m3 codes) or 2 (NVFP4 codes, block scales already applied by the MMA): the
-// accumulator is scaled by the token's and the weight row's scales before the epilogue proper.
+// 32 accumulator columns of this thread's row as floats.  AK = 1 (e4m3 codes) or 2 (NVFP4
+// codes, block scales already applied by the MMA): scaled by the token's and the weight
+// rows' scales; then the bias (may be null).
 template <int AK>
-F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
+F3_DEV void acc_chunk(uint32_t taddr, float (&v)[32], float sa, const float* wsc, const float* bias) {
+    uint32_t t[32];
+    tmem_ld32(taddr, t);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]);
+    if (AK) {
+        const float4* s4 = reinterpret_cast<const float4*>(wsc);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 sw = __ldg(s4 + i);
+            v[4 * i] *= sa * sw.x; v[4 * i + 1] *= sa * sw.y; v[4 * i + 2] *= sa * sw.z; v[4 * i + 3] *= sa * sw.w;
+        }
+    }
+    if (bias) {
+        const float4* b4 = reinterpret_cast<const float4*>(bias);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 b = __ldg(b4 + i);
+            v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
+        }
+    }
+}
+
+// part / nparts: this warp's share of the tile when two warps serve one lane quarter (a
+// QKV tile's heads, a SwiGLU tile's 32-column chunks, interleaved).  A Q or K head is read
+// from TMEM twice, 32 columns at a time: once for the RMS, once to normalise, rotate and
+// store, so a thread holds 32 values rather than the whole head.
+template <int AK, int NPARTS>
+F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid, int part) {
     const int nq = 3 * p.heads / 2;
     const float sa = AK ? p.a_scale[r] : 1.f;
     if (n < nq) {
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = part; hh < 2; hh += NPARTS) {
             const int hg = 2 * n + hh;  // head index in Q | K | V order
             const int kind = hg / p.heads;
             const int head = hg - kind * p.heads;
-            float v[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t t[32];
-                tmem_ld32(tacc + hh * 128 + c * 32, t);
-                tmem_ld_wait();
-                unpack32(t, v + c * 32);
-            }
-            if (!valid) continue;
-            if (AK) {
-                const float4* s4 = reinterpret_cast<const float4*>(w.w_scale + hg * 128);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float4 sw = __ldg(s4 + i);
-                    v[4 * i] *= sa * sw.x; v[4 * i + 1] *= sa * sw.y; v[4 * i + 2] *= sa * sw.z; v[4 * i + 3] *= sa * sw.w;
-                }
-            }
-            if (w.bias) {
-                const float4* b4 = reinterpret_cast<const float4*>(w.bias + hg * 128);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float4 b = __ldg(b4 + i);
-                    v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
-                }
-            }
+            const uint32_t th = tacc + hh * 128;
+            const float* wsc = AK ? w.w_scale + hg * 128 : nullptr;
+            const float* bias = w.bias ? w.bias + hg * 128 : nullptr;
             if (kind < 2) {
                 float ss = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    acc_chunk<AK>(th + c * 32, v, sa, wsc + (AK ? c * 32 : 0), bias ? bias + c * 32 : nullptr);
 #pragma unroll
-                for (int i = 0; i < 128; ++i) ss = fmaf(v[i], v[i], ss);
+                    for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+                }
                 const float inv = rsqrtf(ss * (1.f / 128.f) + p.rms_eps);
                 const float4* g4 = reinterpret_cast<const float4*>(kind == 0 ? w.q_norm : w.k_norm);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float4 g = __ldg(g4 + i);
-                    v[4 * i] *= inv * g.x; v[4 * i + 1] *= inv * g.y; v[4 * i + 2] *= inv * g.z; v[4 * i + 3] *= inv * g.w;
-                }
                 const float4* cs = reinterpret_cast<const float4*>(p.rope + (size_t)r * 128);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {  // two pairs per float4: (cos0, sin0, cos1, sin1)
-                    const float4 c = __ldg(cs + i);
-                    const float a0 = v[4 * i], a1 = v[4 * i + 1], b0 = v[4 * i + 2], b1 = v[4 * i + 3];
-                    v[4 * i] = a0 * c.x - a1 * c.y;
-                    v[4 * i + 1] = a0 * c.y + a1 * c.x;
-                    v[4 * i + 2] = b0 * c.z - b1 * c.w;
-                    v[4 * i + 3] = b0 * c.w + b1 * c.z;
-                }
                 __nv_bfloat16* dst = (kind == 0 ? p.q : p.k) + ((size_t)head * p.n_tokens + r) * 128;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    acc_chunk<AK>(th + c * 32, v, sa, wsc + (AK ? c * 32 : 0), bias ? bias + c * 32 : nullptr);
+                    if (!valid) continue;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    st_global_v4(dst + 8 * i, pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                                 pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 g = __ldg(g4 + c * 8 + i);
+                        v[4 * i] *= inv * g.x; v[4 * i + 1] *= inv * g.y; v[4 * i + 2] *= inv * g.z; v[4 * i + 3] *= inv * g.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {  // two pairs per float4: (cos0, sin0, cos1, sin1)
+                        const float4 e = __ldg(cs + c * 8 + i);
+                        const float a0 = v[4 * i], a1 = v[4 * i + 1], b0 = v[4 * i + 2], b1 = v[4 * i + 3];
+                        v[4 * i] = a0 * e.x - a1 * e.y;
+                        v[4 * i + 1] = a0 * e.y + a1 * e.x;
+                        v[4 * i + 2] = b0 * e.z - b1 * e.w;
+                        v[4 * i + 3] = b0 * e.w + b1 * e.z;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_global_v4(dst + c * 32 + 8 * i, pack_bf16(v[8 * i], v[8 * i + 1]),
+                                     pack_bf16(v[8 * i + 2], v[8 * i + 3]), pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                                     pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+                }
             } else {
                 __nv_bfloat16* dst = p.vt + (size_t)head * 128 * p.ld_vt + r;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    acc_chunk<AK>(th + c * 32, v, sa, wsc + (AK ? c * 32 : 0), bias ? bias + c * 32 : nullptr);
+                    if (!valid) continue;
 #pragma unroll
-                for (int i = 0; i < 128; ++i) dst[(size_t)i * p.ld_vt] = __float2bfloat16_rn(v[i]);
+                    for (int i = 0; i < 32; ++i) dst[(size_t)(c * 32 + i) * p.ld_vt] = __float2bfloat16_rn(v[i]);
+                }
             }
         }
     } else {
@@ -182,26 +211,14 @@ F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
         __nv_bfloat16* dst = p.y + (size_t)r * p.ld_y + p.width + 128 * j;
         const float* bg = w.bias ? w.bias + 3 * p.width + 128 * j : nullptr;
         const float* bu = w.bias ? w.bias + 3 * p.width + p.ffn + 128 * j : nullptr;
+        const float* sg = AK ? w.w_scale + 3 * p.width + 128 * j : nullptr;
+        const float* su = AK ? sg + p.ffn : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            uint32_t tg[32], tu[32];
-            tmem_ld32(tacc + c * 32, tg);
-            tmem_ld32(tacc + 128 + c * 32, tu);
-            tmem_ld_wait();
-            if (!valid) continue;
+        for (int c = part; c < 4; c += NPARTS) {
             float g[32], u[32];
-            unpack32(tg, g);
-            unpack32(tu, u);
-            if (AK) {
-                const float* sg = w.w_scale + 3 * p.width + 128 * j + c * 32;
-                const float* su = sg + p.ffn;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) { g[i] *= sa * __ldg(sg + i); u[i] *= sa * __ldg(su + i); }
-            }
-            if (bg) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) { g[i] += __ldg(bg + c * 32 + i); u[i] += __ldg(bu + c * 32 + i); }
-            }
+            acc_chunk<AK>(tacc + c * 32, g, sa, AK ? sg + c * 32 : nullptr, bg ? bg + c * 32 : nullptr);
+            acc_chunk<AK>(tacc + 128 + c * 32, u, sa, AK ? su + c * 32 : nullptr, bu ? bu + c * 32 : nullptr);
+            if (!valid) continue;
             uint32_t o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -330,10 +347,12 @@ F3_DEV TileInfo tile_info(const GemmParams& p, int task, int rank, int cl) {
 }
 
 // AK: operand kind, 0 = bf16 (64 elements per 128-byte row of a k-block), 1 = e4m3 (128).
-template <int BN, int EPI, int CL, int AK = 0>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+// EW: epilogue warps (4, or 8 for the input projection).
+template <int BN, int EPI, int CL, int AK = 0, int EW = 4>
+__global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
     static_assert(CL == 1 || (CL == 2 && BN == 256), "clusters of two split a 256-row B tile");
     static_assert(AK == 0 || EPI == EPI_QKV_SWIGLU, "e4m3 operands: input projection only");
+    static_assert(EW == 4 || (EW == 8 && EPI == EPI_QKV_SWIGLU), "8 epilogue warps: input projection only");
     constexpr int KB_ELEMS = AK ? 128 : GEMM_BK;
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), EW);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -466,8 +485,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue warps 2..5
+        // ---------------- epilogue warps 2 .. 2 + EW - 1
         const int sub = warp & 3;  // TMEM lane quarter this warp may access
+        const int part = (warp - 2) >> 2;
         int acc = 0;
         uint32_t aph = 0;
         for (int task = unit; task < tasks; task += n_units) {
@@ -478,7 +498,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tcgen05_kernel(const __g
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16) + acc * BN;
             const EpiWeights& w = p.ew[p.grp[ti.g].wset];
-            if (EPI == EPI_QKV_SWIGLU) epi_qkv<AK>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            if (EPI == EPI_QKV_SWIGLU) epi_qkv<AK, EW / 4>(p, w, ti.n, tacc, valid ? r : 0, valid, part);
             else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_F32) epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);

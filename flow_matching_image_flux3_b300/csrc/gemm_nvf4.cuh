@@ -5,7 +5,8 @@
 // for each operand row) and the same fused epilogue as the bf16 input projection.
 //
 // The same persistent, warp-specialised structure as gemm_tcgen05_kernel (warp 0 TMA,
-// warp 1 MMA, warps 2..5 epilogue; clusters of two share the weight tile by multicast),
+// warp 1 MMA, EW epilogue warps from warp 2; clusters of two share the weight tile by
+// multicast),
 // with two differences:
 //  - a stage also carries the tiles' block scales (2 KB for the 128 A rows, 4 KB for the
 //    256 B rows of a 256-element k-block, 1-D bulk copies of the tiled scale layout), and
@@ -36,9 +37,10 @@ struct Nvf4Cfg {
     static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
 };
 
-template <int CL>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_nvf4_kernel(const __grid_constant__ GemmParams p) {
+template <int CL, int EW>
+__global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_nvf4_kernel(const __grid_constant__ GemmParams p) {
     static_assert(CL == 1 || CL == 2, "clusters of one or two");
+    static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
     using C = Nvf4Cfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -63,7 +65,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_nvf4_kernel(const __grid
             mbar_init(empty_bar(s), CL);
         }
         mbar_init(tfull_bar, 1);
-        mbar_init(tempty_bar, 4);
+        mbar_init(tempty_bar, EW);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -180,8 +182,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_nvf4_kernel(const __grid
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue warps 2..5
+        // ---------------- epilogue warps 2 .. 2 + EW - 1
         const int sub = warp & 3;
+        const int part = (warp - 2) >> 2;
         uint32_t aph = 0;
         for (int task = unit; task < tasks; task += n_units) {
             const TileInfo ti = tile_info(p, task, rank, CL);
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_nvf4_kernel(const __grid
             if (!mbar_wait_warp(tfull_bar, aph, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16);
-            epi_qkv<2>(p, p.ew[p.grp[ti.g].wset], ti.n, tacc, valid ? r : 0, valid);
+            epi_qkv<2, EW / 4>(p, p.ew[p.grp[ti.g].wset], ti.n, tacc, valid ? r : 0, valid, part);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar);
