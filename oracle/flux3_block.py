@@ -225,6 +225,19 @@ def _in_proj(a: np.ndarray, w: "Weights", quant: Optional[str]) -> np.ndarray:
     return a @ w.w_in.T + w.b_in
 
 
+def _out_proj(ycat: np.ndarray, w: "Weights", quant: Optional[str]) -> np.ndarray:
+    """y = [attn | act] W_out^T + b_out; quant "fp8" / "nvfp4": the product on quantized
+    operands (the rows of [attn | act] and of W_out, as for the input projection)."""
+    if quant == "fp8":
+        from .fp8 import fp8_linear
+        return fp8_linear(ycat, w.w_out) + w.b_out
+    if quant == "nvfp4":
+        from .nvfp4 import nvfp4_linear
+        return nvfp4_linear(ycat, w.w_out) + w.b_out
+    assert quant is None
+    return ycat @ w.w_out.T + w.b_out
+
+
 def _quant(fp8_in_proj: bool, nvfp4_in_proj: bool) -> Optional[str]:
     assert not (fp8_in_proj and nvfp4_in_proj)
     return "fp8" if fp8_in_proj else ("nvfp4" if nvfp4_in_proj else None)
@@ -233,7 +246,8 @@ def _quant(fp8_in_proj: bool, nvfp4_in_proj: bool) -> Optional[str]:
 def block_forward(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int], mod: np.ndarray,
                   angles: np.ndarray, heads: int, head_dim: int = 128, ln_eps: float = 1e-6,
                   rms_eps: float = 1e-6, stage: int = 2, rounding: Optional[str] = None,
-                  fp8_in_proj: bool = False, nvfp4_in_proj: bool = False) -> BlockOut:
+                  fp8_in_proj: bool = False, nvfp4_in_proj: bool = False,
+                  out_proj_quant: Optional[str] = None) -> BlockOut:
     """One transformer block.
 
     stage 2 (joint): one weight set, attention over all tokens, modulation per stream.
@@ -241,7 +255,8 @@ def block_forward(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int],
     rounding="bf16" rounds to bf16 where the device stores bf16 tensors (the modulated
     input, q, k, v, the attention output, the SwiGLU output and x'); None keeps fp64.
     fp8_in_proj: the input projection on row-wise e4m3 operands (oracle/fp8.py);
-    nvfp4_in_proj: on NVFP4 operands (oracle/nvfp4.py)."""
+    nvfp4_in_proj: on NVFP4 operands (oracle/nvfp4.py); out_proj_quant "fp8" / "nvfp4":
+    the output projection on quantized operands too."""
     x = np.asarray(x, dtype=F64)
     n, D = x.shape
     H, d = heads, head_dim
@@ -273,7 +288,7 @@ def block_forward(x: np.ndarray, weights: List[Weights], seg_off: Sequence[int],
     ycat = np.concatenate([attn, act], axis=1)
     y = np.empty((n, D))
     for lo, hi, w in rows:
-        y[lo:hi] = ycat[lo:hi] @ w.w_out.T + w.b_out
+        y[lo:hi] = _out_proj(ycat[lo:hi], w, out_proj_quant)
     gate = mod[segment_ids(seg_off), 2]
     x_out = _maybe_round(x + gate * y, rounding)
     r.a, r.q, r.k, r.v, r.attn, r.act, r.y, r.x_out = a, q, k, v, attn, act, y, x_out
@@ -348,7 +363,7 @@ def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[
                        angles: np.ndarray, heads: int, rows: Sequence[int], head_dim: int = 128,
                        ln_eps: float = 1e-6, rms_eps: float = 1e-6, stage: int = 2,
                        rounding: Optional[str] = None, kv=None, fp8_in_proj: bool = False,
-                       nvfp4_in_proj: bool = False) -> dict:
+                       nvfp4_in_proj: bool = False, out_proj_quant: Optional[str] = None) -> dict:
     """The block's outputs for a few rows, at sizes where the whole block is too slow.
 
     A row's output needs its own q, gate/up and the keys and values of every token it
@@ -392,7 +407,7 @@ def block_forward_rows(x: np.ndarray, weights: List[Weights], seg_off: Sequence[
             o[:, h] = (e / e.sum(axis=1, keepdims=True)) @ vh[h, lo:hi]
         o = _maybe_round(o.reshape(len(rr), -1), rounding)
         act = _maybe_round(swiglu(p[:, 3 * D:3 * D + F], p[:, 3 * D + F:3 * D + 2 * F]), rounding)
-        y = np.concatenate([o, act], axis=1) @ w.w_out.T + w.b_out
+        y = _out_proj(np.concatenate([o, act], axis=1), w, out_proj_quant)
         xo = _maybe_round(x[rr] + mod[seg[rr], 2] * y, rounding)
         for j, i in enumerate(idx):
             res["q"][i], res["attn"][i], res["act"][i], res["x_out"][i] = q[j], o[j], act[j], xo[j]

@@ -124,3 +124,38 @@ def test_storage_layout_inverse_and_packing():
     codes = rng.integers(0, 16, size=(3, 64)).astype(np.uint8)
     assert (Q.unpack_codes(Q.pack_codes(codes)) == codes).all()
     assert Q.pack_codes(np.array([[1, 2]], dtype=np.uint8))[0, 0] == 0x21
+
+
+def _tiny_block_args():
+    import oracle as O
+    from flow_matching_image_flux3_b300 import synth
+    case = synth.config(0, bias=True)
+    d = case.dims
+    ang = O.rope_angles(case.pos.numpy(), d.rope_theta)
+    w = [O.Weights(*(synth.as_f64(t) for t in (wi.w_in, wi.b_in, wi.q_norm, wi.k_norm, wi.w_out, wi.b_out)))
+         for wi in case.weights]
+    return O, (synth.as_f64(case.x), w, case.seg_off, synth.as_f64(case.mod), ang, d.heads)
+
+
+@pytest.mark.parametrize("quant", ["fp8", "nvfp4"])
+def test_quantized_block_rows_match_quantized_block(quant):
+    # the sampled-rows path takes the same steps as the whole block, both projections quantized
+    O, args = _tiny_block_args()
+    kw = dict(rounding="bf16", out_proj_quant=quant, **({"fp8_in_proj": True} if quant == "fp8" else {"nvfp4_in_proj": True}))
+    full = O.block_forward(*args, **kw)
+    rows = [0, 5, 63, 64, 143]
+    part = O.block_forward_rows(*args, rows, **kw)
+    np.testing.assert_allclose(part["x_out"], full.x_out[rows], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("quant", ["fp8", "nvfp4"])
+def test_quantized_block_is_close_to_the_bf16_block(quant):
+    # not a pin of the arithmetic (the tests above are): quantizing both projections moves y
+    # by a few percent (fp8) to ~10-20% (nvfp4) and x' by far less, since x dominates it
+    O, args = _tiny_block_args()
+    ref = O.block_forward(*args, rounding="bf16")
+    kw = {"fp8_in_proj": True} if quant == "fp8" else {"nvfp4_in_proj": True}
+    qb = O.block_forward(*args, rounding="bf16", out_proj_quant=quant, **kw)
+    e_y = np.linalg.norm(qb.y - ref.y) / np.linalg.norm(ref.y)
+    assert 1e-3 < e_y < (0.1 if quant == "fp8" else 0.3)
+    assert np.linalg.norm(qb.x_out - ref.x_out) / np.linalg.norm(ref.x_out) < (2e-2 if quant == "fp8" else 0.1)
