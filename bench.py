@@ -470,10 +470,10 @@ def run_workload(args):
         x_out = torch.empty_like(x)
         wsp = B.workspace(B.block_workspace_size(d, N), dev)
 
-        w8 = B.Fp8Weights(ws_[0]) if args.workload == "joint_fp8" else None
+        w8 = B.Fp8Weights(ws_[0], quantize_out=True) if args.workload == "joint_fp8" else None
         if w8 is not None:
             wsp = B.workspace(B.block_fp8_workspace_size(d, N), dev)
-        w4 = B.Nvfp4Weights(ws_[0]) if args.workload == "joint_nvfp4" else None
+        w4 = B.Nvfp4Weights(ws_[0], quantize_out=True) if args.workload == "joint_nvfp4" else None
         if w4 is not None:
             wsp = B.workspace(B.block_nvfp4_workspace_size(d, N), dev)
 

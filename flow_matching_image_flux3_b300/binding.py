@@ -34,12 +34,12 @@ class flux3_block_weights(ctypes.Structure):
 
 class flux3_block_weights_fp8(ctypes.Structure):
     _fields_ = [("w_in", c_vp), ("s_in", c_vp), ("b_in", c_vp), ("q_norm", c_vp), ("k_norm", c_vp), ("w_out", c_vp),
-                ("b_out", c_vp)]
+                ("b_out", c_vp), ("w_out_q", c_vp), ("s_out", c_vp)]
 
 
 class flux3_block_weights_nvfp4(ctypes.Structure):
     _fields_ = [("w_in", c_vp), ("w_sf", c_vp), ("s_in", c_vp), ("b_in", c_vp), ("q_norm", c_vp), ("k_norm", c_vp),
-                ("w_out", c_vp), ("b_out", c_vp)]
+                ("w_out", c_vp), ("b_out", c_vp), ("w_out_q", c_vp), ("w_out_sf", c_vp), ("s_out", c_vp)]
 
 
 class flux3_segments(ctypes.Structure):
@@ -454,19 +454,22 @@ def quantize_rows_fp8(x: torch.Tensor, stream=None):
 
 
 class Fp8Weights:
-    """A block's weights with the input projection quantized row-wise to e4m3 (on the
-    device, through flux3_quantize_rows_fp8); W_out, norms and biases as given."""
+    """A block's weights with the input projection (and with quantize_out the output
+    projection too) quantized row-wise to e4m3 on the device (flux3_quantize_rows_fp8);
+    norms and biases as given."""
 
-    def __init__(self, w, stream=None):
+    def __init__(self, w, stream=None, quantize_out: bool = False):
         self.w_in, self.s_in = quantize_rows_fp8(w.w_in, stream)
         self.b_in, self.q_norm, self.k_norm = w.b_in, w.q_norm, w.k_norm
         self.w_out, self.b_out = w.w_out, w.b_out
+        self.w_out_q, self.s_out = quantize_rows_fp8(w.w_out, stream) if quantize_out else (None, None)
 
 
 def _fp8_struct(w: Fp8Weights) -> flux3_block_weights_fp8:
     return flux3_block_weights_fp8(_ptr(w.w_in, torch.uint8), _ptr(w.s_in, torch.float32), _ptr(w.b_in, torch.float32),
                                    _ptr(w.q_norm, torch.float32), _ptr(w.k_norm, torch.float32),
-                                   _ptr(w.w_out, torch.bfloat16), _ptr(w.b_out, torch.float32))
+                                   _ptr(w.w_out, torch.bfloat16), _ptr(w.b_out, torch.float32),
+                                   _ptr(w.w_out_q, torch.uint8), _ptr(w.s_out, torch.float32))
 
 
 def in_proj_fp8_fwd(dims, weights: Sequence[Fp8Weights], seg_off: Sequence[int], a8: torch.Tensor, sa: torch.Tensor,
@@ -526,20 +529,24 @@ def quantize_rows_nvfp4(x: torch.Tensor, stream=None):
 
 
 class Nvfp4Weights:
-    """A block's weights with the input projection quantized to NVFP4 (on the device,
-    through flux3_quantize_rows_nvfp4); W_out, norms and biases as given."""
+    """A block's weights with the input projection (and with quantize_out the output
+    projection too) quantized to NVFP4 on the device (flux3_quantize_rows_nvfp4); norms
+    and biases as given."""
 
-    def __init__(self, w, stream=None):
+    def __init__(self, w, stream=None, quantize_out: bool = False):
         self.w_in, self.w_sf, self.s_in = quantize_rows_nvfp4(w.w_in, stream)
         self.b_in, self.q_norm, self.k_norm = w.b_in, w.q_norm, w.k_norm
         self.w_out, self.b_out = w.w_out, w.b_out
+        self.w_out_q, self.w_out_sf, self.s_out = (quantize_rows_nvfp4(w.w_out, stream) if quantize_out
+                                                   else (None, None, None))
 
 
 def _nvfp4_struct(w: Nvfp4Weights) -> flux3_block_weights_nvfp4:
     return flux3_block_weights_nvfp4(_ptr(w.w_in, torch.uint8), _ptr(w.w_sf, torch.uint8), _ptr(w.s_in, torch.float32),
                                      _ptr(w.b_in, torch.float32), _ptr(w.q_norm, torch.float32),
                                      _ptr(w.k_norm, torch.float32), _ptr(w.w_out, torch.bfloat16),
-                                     _ptr(w.b_out, torch.float32))
+                                     _ptr(w.b_out, torch.float32), _ptr(w.w_out_q, torch.uint8),
+                                     _ptr(w.w_out_sf, torch.uint8), _ptr(w.s_out, torch.float32))
 
 
 def in_proj_nvfp4_fwd(dims, weights: Nvfp4Weights, a4: torch.Tensor, a_sf: torch.Tensor, sa: torch.Tensor,

@@ -385,7 +385,8 @@ flux3_status run_in_proj_nvfp4(const flux3_dims* d, const flux3_block_weights_nv
     P.rope = rope;
     P.q = static_cast<__nv_bfloat16*>(q); P.k = static_cast<__nv_bfloat16*>(k);
     P.vt = static_cast<__nv_bfloat16*>(vt); P.y = static_cast<__nv_bfloat16*>(y);
-    return launch_pairs<gemm_nvf4_kernel<2, 8>>(P, Nvf4Cfg::SMEM_BYTES, gemm_threads(8), st, FLUX3_KERNEL_IN_PROJ);
+    return launch_pairs<gemm_nvf4_kernel<2, 8, EPI_QKV_SWIGLU>>(P, Nvf4Cfg::SMEM_BYTES, gemm_threads(8), st,
+                                                               FLUX3_KERNEL_IN_PROJ);
 }
 
 // rows padded to a pair of 128-row tiles: the scale rows an NVFP4 GEMM may read
@@ -423,6 +424,41 @@ flux3_status run_out_proj(const flux3_dims* d, const flux3_block_weights* w, int
     P.n_seg = segs->n_seg;
     for (int i = 0; i <= segs->n_seg; ++i) P.seg_off[i] = segs->seg_off[i];
     return launch_gemm<256, EPI_GATED_RESIDUAL, 2>(P, st, FLUX3_KERNEL_OUT_PROJ);
+}
+
+// the output projection with the gated residual on quantized operands (one weight set):
+// y_q [N, K] codes of [attention | SwiGLU] (K = D + F; e4m3: K bytes per row, NVFP4: K / 2
+// with tiled block scales y_sf), sy their per-token scales; w_q W_out's codes [D, ...],
+// w_sf its block scales (NVFP4), s_w its row scales
+flux3_status run_out_proj_quant(const flux3_dims* d, bool nvfp4, const void* w_q, const void* w_sf, const float* s_w,
+                                const float* b_out, const flux3_segments* segs, const void* y_q, const void* y_sf,
+                                const float* sy, const void* x, void* x_out, int N, cudaStream_t st) {
+    if (N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    const int D = d->width, F = d->ffn_hidden;
+    const int K = D + F;
+    const uint64_t row = nvfp4 ? (uint64_t)K / 2 : (uint64_t)K;
+    if (!tmap_2d_u8(&P.tm_a, y_q, row, N, row, 128)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_2d_u8(&P.tm_b[0], w_q, row, D, row, 128)) return FLUX3_ERR_INVALID_ARG;
+    P.ew[0] = {b_out, nullptr, nullptr, s_w, static_cast<const uint8_t*>(w_sf)};
+    const int32_t one[2] = {0, N};
+    fill_groups(P, one, 1, 1, N, 2);
+    P.n_tiles = D / 256;
+    P.k_blocks = nvfp4 ? K / 256 : K / 128;
+    P.sf_steps = K / 64;
+    P.a_scale = sy;
+    P.a_sf = static_cast<const uint8_t*>(y_sf);
+    P.width = D;
+    P.x = static_cast<const __nv_bfloat16*>(x);
+    P.x_out = static_cast<__nv_bfloat16*>(x_out);
+    P.mod = segs->mod;
+    P.n_seg = segs->n_seg;
+    for (int i = 0; i <= segs->n_seg; ++i) P.seg_off[i] = segs->seg_off[i];
+    if (nvfp4)
+        return launch_pairs<gemm_nvf4_kernel<2, 4, EPI_GATED_RESIDUAL>>(P, Nvf4Cfg::SMEM_BYTES, gemm_threads(4), st,
+                                                                        FLUX3_KERNEL_OUT_PROJ);
+    return launch_gemm<256, EPI_GATED_RESIDUAL, 2, 1>(P, st, FLUX3_KERNEL_OUT_PROJ);
 }
 
 flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const void* vt, int ld_vt, int N, const int32_t* off,
@@ -1045,10 +1081,38 @@ flux3_status flux3_in_proj_fp8_fwd(const flux3_dims* dims, const flux3_block_wei
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// the quantized block's scratch after the bf16 block's: the input projection's codes,
+// block scales (NVFP4) and row scales, then the output projection's
+struct QuantWs {
+    uint8_t *a_q, *a_sf, *y_q, *y_sf;
+    float *sa, *sy;
+    size_t bytes;
+};
+QuantWs quant_ws(const flux3_dims* d, int N, bool nvfp4, uint8_t* base) {
+    const int D = d->width, K = d->width + d->ffn_hidden;
+    QuantWs w;
+    size_t off = block_ws_layout(d, N, nullptr).bytes;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? base + off : nullptr;
+        off += up256(bytes);
+        return p;
+    };
+    const size_t rp = (size_t)nvfp4_rows_padded(N);
+    w.a_q = take((size_t)N * (nvfp4 ? D / 2 : D));
+    w.a_sf = nvfp4 ? take(rp * (D / 16)) : nullptr;
+    w.sa = reinterpret_cast<float*>(take((size_t)N * 4));
+    w.y_q = take((size_t)N * (nvfp4 ? K / 2 : K));
+    w.y_sf = nvfp4 ? take(rp * (K / 16)) : nullptr;
+    w.sy = reinterpret_cast<float*>(take((size_t)N * 4));
+    w.bytes = off;
+    return w;
+}
+}  // namespace
+
 size_t flux3_block_fp8_workspace_size(const flux3_dims* dims, int32_t n_tokens) {
     if (check_dims(dims) != FLUX3_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
-    return block_ws_layout(dims, n_tokens, nullptr).bytes + up256((size_t)n_tokens * dims->width) +
-           up256((size_t)n_tokens * 4);
+    return quant_ws(dims, n_tokens, false, nullptr).bytes;
 }
 
 flux3_status flux3_block_fp8_fwd(const flux3_dims* dims, const flux3_block_weights_fp8* w, const flux3_segments* segs,
@@ -1061,21 +1125,28 @@ flux3_status flux3_block_fp8_fwd(const flux3_dims* dims, const flux3_block_weigh
     if (N < 0 || N > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
     if ((s = check_segs(segs, N, true)) != FLUX3_OK) return s;
     if ((s = check_weights_fp8(w, 1)) != FLUX3_OK) return s;
-    if (!w->w_out || !al16(w->w_out) || (w->b_out && !al16(w->b_out))) return FLUX3_ERR_INVALID_ARG;
+    if (w->b_out && !al16(w->b_out)) return FLUX3_ERR_INVALID_ARG;
+    if (w->w_out_q ? (!al16(w->w_out_q) || !w->s_out) : (!w->w_out || !al16(w->w_out))) return FLUX3_ERR_INVALID_ARG;
+    if ((dims->width + dims->ffn_hidden) % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
     if (N == 0) return FLUX3_OK;
     if (!x || !x_out || !rope || !al16(x) || !al16(x_out) || !al16(rope)) return FLUX3_ERR_INVALID_ARG;
     if (!ws || !al256(ws) || ws_bytes < flux3_block_fp8_workspace_size(dims, N)) return FLUX3_ERR_WORKSPACE;
     if (!have_encode()) return FLUX3_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const BlockWs b = block_ws_layout(dims, N, static_cast<uint8_t*>(ws));
-    uint8_t* a8 = static_cast<uint8_t*>(ws) + b.bytes;
-    float* sa = reinterpret_cast<float*>(a8 + up256((size_t)N * dims->width));
+    const QuantWs qw = quant_ws(dims, N, false, static_cast<uint8_t*>(ws));
     const int D = dims->width, F = dims->ffn_hidden;
     if ((s = run_adaln(dims, segs->mod, seg_table(segs->seg_off, segs->n_seg), x, N, b.a, st)) != FLUX3_OK) return s;
-    if ((s = run_quantize_rows(b.a, N, D, a8, sa, st)) != FLUX3_OK) return s;
-    if ((s = run_in_proj_fp8(dims, w, 1, segs, a8, sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK) return s;
+    if ((s = run_quantize_rows(b.a, N, D, qw.a_q, qw.sa, st)) != FLUX3_OK) return s;
+    if ((s = run_in_proj_fp8(dims, w, 1, segs, qw.a_q, qw.sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK)
+        return s;
     const int32_t full[2] = {0, N};
     if ((s = run_attn(dims, b.q, b.k, b.vt, b.ld_vt, N, full, 1, b.y, D + F, false, st)) != FLUX3_OK) return s;
+    if (w->w_out_q) {
+        if ((s = run_quantize_rows(b.y, N, D + F, qw.y_q, qw.sy, st)) != FLUX3_OK) return s;
+        return run_out_proj_quant(dims, false, w->w_out_q, nullptr, w->s_out, w->b_out, segs, qw.y_q, nullptr, qw.sy, x,
+                                  x_out, N, st);
+    }
     const flux3_block_weights wo{nullptr, nullptr, nullptr, nullptr, w->w_out, w->b_out};
     return run_out_proj(dims, &wo, 1, segs, b.y, x, x_out, N, st);
 }
@@ -1118,30 +1189,9 @@ flux3_status flux3_in_proj_nvfp4_fwd(const flux3_dims* dims, const flux3_block_w
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
-namespace {
-struct Nvfp4Ws {
-    uint8_t *a4, *sf;
-    float* sa;
-    size_t bytes;
-};
-Nvfp4Ws block_nvfp4_ws(const flux3_dims* d, int N, uint8_t* base) {
-    const BlockWs b = block_ws_layout(d, N, nullptr);
-    Nvfp4Ws w;
-    size_t off = b.bytes;
-    w.a4 = base ? base + off : nullptr;
-    off += up256((size_t)N * d->width / 2);
-    w.sf = base ? base + off : nullptr;
-    off += up256((size_t)nvfp4_rows_padded(N) * (d->width / 16));
-    w.sa = base ? reinterpret_cast<float*>(base + off) : nullptr;
-    off += up256((size_t)N * 4);
-    w.bytes = off;
-    return w;
-}
-}  // namespace
-
 size_t flux3_block_nvfp4_workspace_size(const flux3_dims* dims, int32_t n_tokens) {
     if (check_dims(dims) != FLUX3_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
-    return block_nvfp4_ws(dims, n_tokens, nullptr).bytes;
+    return quant_ws(dims, n_tokens, true, nullptr).bytes;
 }
 
 flux3_status flux3_block_nvfp4_fwd(const flux3_dims* dims, const flux3_block_weights_nvfp4* w, const flux3_segments* segs,
@@ -1154,21 +1204,30 @@ flux3_status flux3_block_nvfp4_fwd(const flux3_dims* dims, const flux3_block_wei
     if (N < 0 || N > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
     if ((s = check_segs(segs, N, true)) != FLUX3_OK) return s;
     if ((s = check_weights_nvfp4(w)) != FLUX3_OK) return s;
-    if (!w->w_out || !al16(w->w_out) || (w->b_out && !al16(w->b_out))) return FLUX3_ERR_INVALID_ARG;
+    if (w->b_out && !al16(w->b_out)) return FLUX3_ERR_INVALID_ARG;
+    if (w->w_out_q ? (!al16(w->w_out_q) || !w->w_out_sf || !al16(w->w_out_sf) || !w->s_out)
+                   : (!w->w_out || !al16(w->w_out)))
+        return FLUX3_ERR_INVALID_ARG;
+    if ((dims->width + dims->ffn_hidden) % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
     if (N == 0) return FLUX3_OK;
     if (!x || !x_out || !rope || !al16(x) || !al16(x_out) || !al16(rope)) return FLUX3_ERR_INVALID_ARG;
     if (!ws || !al256(ws) || ws_bytes < flux3_block_nvfp4_workspace_size(dims, N)) return FLUX3_ERR_WORKSPACE;
     if (!have_encode()) return FLUX3_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const BlockWs b = block_ws_layout(dims, N, static_cast<uint8_t*>(ws));
-    const Nvfp4Ws nw = block_nvfp4_ws(dims, N, static_cast<uint8_t*>(ws));
+    const QuantWs qw = quant_ws(dims, N, true, static_cast<uint8_t*>(ws));
     const int D = dims->width, F = dims->ffn_hidden;
     if ((s = run_adaln(dims, segs->mod, seg_table(segs->seg_off, segs->n_seg), x, N, b.a, st)) != FLUX3_OK) return s;
-    if ((s = run_quantize_rows_nvfp4(b.a, N, D, nw.a4, nw.sf, nw.sa, st)) != FLUX3_OK) return s;
-    if ((s = run_in_proj_nvfp4(dims, w, nw.a4, nw.sf, nw.sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK)
+    if ((s = run_quantize_rows_nvfp4(b.a, N, D, qw.a_q, qw.a_sf, qw.sa, st)) != FLUX3_OK) return s;
+    if ((s = run_in_proj_nvfp4(dims, w, qw.a_q, qw.a_sf, qw.sa, N, rope, b.q, b.k, b.vt, b.ld_vt, b.y, st)) != FLUX3_OK)
         return s;
     const int32_t full[2] = {0, N};
     if ((s = run_attn(dims, b.q, b.k, b.vt, b.ld_vt, N, full, 1, b.y, D + F, false, st)) != FLUX3_OK) return s;
+    if (w->w_out_q) {
+        if ((s = run_quantize_rows_nvfp4(b.y, N, D + F, qw.y_q, qw.y_sf, qw.sy, st)) != FLUX3_OK) return s;
+        return run_out_proj_quant(dims, true, w->w_out_q, w->w_out_sf, w->s_out, w->b_out, segs, qw.y_q, qw.y_sf, qw.sy, x,
+                                  x_out, N, st);
+    }
     const flux3_block_weights wo{nullptr, nullptr, nullptr, nullptr, w->w_out, w->b_out};
     return run_out_proj(dims, &wo, 1, segs, b.y, x, x_out, N, st);
 }

@@ -232,8 +232,11 @@ F3_DEV void epi_qkv(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
     }
 }
 
-template <int BN>
+// AK != 0: the operands were quantized codes; the accumulator is scaled by the token's
+// and the weight rows' scales first.
+template <int BN, int AK>
 F3_DEV void epi_gated_residual(const GemmParams& p, const EpiWeights& w, int n, uint32_t tacc, int r, bool valid) {
+    const float sa = AK ? p.a_scale[r] : 1.f;
     int seg = 0;
 #pragma unroll 1
     for (int s = 1; s < p.n_seg; ++s)
@@ -249,6 +252,10 @@ F3_DEV void epi_gated_residual(const GemmParams& p, const EpiWeights& w, int n, 
         const int col = n * BN + c * 32;
         float a[32];
         unpack32(t, a);
+        if (AK) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] *= sa * __ldg(w.w_scale + col + i);
+        }
         if (w.bias) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
@@ -351,7 +358,7 @@ F3_DEV TileInfo tile_info(const GemmParams& p, int task, int rank, int cl) {
 template <int BN, int EPI, int CL, int AK = 0, int EW = 4>
 __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
     static_assert(CL == 1 || (CL == 2 && BN == 256), "clusters of two split a 256-row B tile");
-    static_assert(AK == 0 || EPI == EPI_QKV_SWIGLU, "e4m3 operands: input projection only");
+    static_assert(AK == 0 || EPI == EPI_QKV_SWIGLU || EPI == EPI_GATED_RESIDUAL, "e4m3 operands: the projections");
     static_assert(EW == 4 || (EW == 8 && EPI == EPI_QKV_SWIGLU), "8 epilogue warps: input projection only");
     constexpr int KB_ELEMS = AK ? 128 : GEMM_BK;
     using C = GemmCfg<BN>;
@@ -499,7 +506,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_tcgen05_kernel(const
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16) + acc * BN;
             const EpiWeights& w = p.ew[p.grp[ti.g].wset];
             if (EPI == EPI_QKV_SWIGLU) epi_qkv<AK, EW / 4>(p, w, ti.n, tacc, valid ? r : 0, valid, part);
-            else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN, AK>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_F32) epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             tc_fence_before();

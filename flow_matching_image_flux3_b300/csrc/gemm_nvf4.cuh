@@ -1,8 +1,9 @@
-// gemm_nvf4.cuh -- the input projection on NVFP4 operands ("FLUX.3" cookbook, section 3,
+// gemm_nvf4.cuh -- the block's projections on NVFP4 operands ("FLUX.3" cookbook, section 3,
 // Quantized checkpoints: FP4 (E2M1) values with FP8 block scales on a Blackwell GPU):
-//   P = s_a[token] * sum_k (e2m1(a) sb_a)(e2m1(w) sb_w) * s_w[out] + b_in
+//   P = s_a[token] * sum_k (e2m1(a) sb_a)(e2m1(w) sb_w) * s_w[out] + b
 // with the block-scaled tcgen05 MMA (kind::mxf4nvf4, one e4m3 scale per 16 elements of K
-// for each operand row) and the same fused epilogue as the bf16 input projection.
+// for each operand row) and the same fused epilogues as the bf16 projections (EPI:
+// EPI_QKV_SWIGLU for the input projection, EPI_GATED_RESIDUAL for the output projection).
 //
 // The same persistent, warp-specialised structure as gemm_tcgen05_kernel (warp 0 TMA,
 // warp 1 MMA, EW epilogue warps from warp 2; clusters of two share the weight tile by
@@ -37,10 +38,11 @@ struct Nvf4Cfg {
     static_assert(ACC_COLS + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
 };
 
-template <int CL, int EW>
+template <int CL, int EW, int EPI>
 __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_nvf4_kernel(const __grid_constant__ GemmParams p) {
     static_assert(CL == 1 || CL == 2, "clusters of one or two");
-    static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
+    static_assert(EPI == EPI_QKV_SWIGLU || EPI == EPI_GATED_RESIDUAL, "the block's projections");
+    static_assert(EW == 4 || (EW == 8 && EPI == EPI_QKV_SWIGLU), "8 epilogue warps: input projection only");
     using C = Nvf4Cfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_nvf4_kernel(const __
             const int ws = p.grp[ti.g].wset;
             const CUtensorMap* tb = &p.tm_b[ws];
             int r0, r1;
-            b_rows<256, EPI_QKV_SWIGLU>(p, ti.n, r0, r1);
+            b_rows<256, EPI>(p, ti.n, r0, r1);
             const uint8_t* sfa = p.a_sf + (size_t)(ti.row0 / GEMM_BM) * sf_row_tile;
             const uint8_t* sfb0 = p.ew[ws].w_sf + (size_t)(r0 / 128) * sf_row_tile;
             const uint8_t* sfb1 = p.ew[ws].w_sf + (size_t)(r1 / 128) * sf_row_tile;
@@ -193,7 +195,10 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_nvf4_kernel(const __
             if (!mbar_wait_warp(tfull_bar, aph, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(sub * 32) << 16);
-            epi_qkv<2, EW / 4>(p, p.ew[p.grp[ti.g].wset], ti.n, tacc, valid ? r : 0, valid, part);
+            if constexpr (EPI == EPI_QKV_SWIGLU)
+                epi_qkv<2, EW / 4>(p, p.ew[p.grp[ti.g].wset], ti.n, tacc, valid ? r : 0, valid, part);
+            else
+                epi_gated_residual<256, 2>(p, p.ew[p.grp[ti.g].wset], ti.n, tacc, valid ? r : 0, valid);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar);

@@ -312,8 +312,8 @@ flux3_status flux3_sample_fwd(const flux3_dims *dims, const flux3_dit_weights *w
  * page, section 3: "fp8 rowwise").  Here the input projection multiplies e4m3 codes on
  * the tensor cores (kind::f8f6f4) with fp32 accumulation:
  *   P = s_a[token] * (a_q W_q^T)[token, out] * s_w[out] + b_in
- * then the same epilogues as flux3_in_proj_fwd.  The output projection stays bf16.
- * Quantization (flux3_quantize_rows_fp8) is per row: scale = amax / 448, codes =
+ * then the same epilogues as flux3_in_proj_fwd; the block entry point can run the output
+ * projection the same way.  Quantization (flux3_quantize_rows_fp8) is per row: scale = amax / 448, codes =
  * e4m3(x * (448 / amax)) rounded to nearest even, saturated at +-448, all in fp32
  * (an all-zero row: zero codes, scale 0).  NVFP4: below. */
 
@@ -322,9 +322,12 @@ flux3_status flux3_sample_fwd(const flux3_dims *dims, const flux3_dit_weights *w
 flux3_status flux3_quantize_rows_fp8(const void *x, int32_t rows, int32_t k, void *q, float *scale,
                                      flux3_stream_t stream);
 
-/* One block's parameters with an e4m3 input projection (device memory).
- *  w_in   uint8 [3D + 2F, D]: e4m3 codes of W_in (rows Q | K | V | gate | up), quantized
- *         per row (flux3_quantize_rows_fp8);  s_in  fp32 [3D + 2F]: their scales.
+/* One block's parameters with e4m3 projections (device memory).
+ *  w_in    uint8 [3D + 2F, D]: e4m3 codes of W_in (rows Q | K | V | gate | up), quantized
+ *          per row (flux3_quantize_rows_fp8);  s_in  fp32 [3D + 2F]: their scales.
+ *  w_out_q uint8 [D, D + F]: e4m3 codes of W_out, s_out fp32 [D] their row scales; when
+ *          set, the block quantizes [attention | SwiGLU] per token and runs the output
+ *          projection on e4m3 operands too; when NULL it runs in bf16 on w_out.
  *  Other fields as flux3_block_weights. */
 typedef struct flux3_block_weights_fp8 {
     const void *w_in;
@@ -334,6 +337,8 @@ typedef struct flux3_block_weights_fp8 {
     const float *k_norm;
     const void *w_out;
     const float *b_out;
+    const void *w_out_q;
+    const float *s_out;
 } flux3_block_weights_fp8;
 
 /* flux3_in_proj_fwd on e4m3 operands: a8  device uint8 [N, D] codes of the modulated input,
@@ -346,10 +351,11 @@ flux3_status flux3_in_proj_fp8_fwd(const flux3_dims *dims, const flux3_block_wei
 
 size_t flux3_block_fp8_workspace_size(const flux3_dims *dims, int32_t n_tokens);
 
-/* The joint block (stage 2) with the e4m3 input projection: LayerNorm + modulation (bf16),
- * row quantization, FP8 input projection with its epilogues, attention, bf16 output
- * projection with the gated residual.  Arguments as flux3_block_fwd; workspace
- * flux3_block_fp8_workspace_size bytes. */
+/* The joint block (stage 2) with e4m3 projections: LayerNorm + modulation (bf16), row
+ * quantization, FP8 input projection with its epilogues, attention, then (w_out_q set)
+ * row quantization of [attention | SwiGLU] and the FP8 output projection, or (w_out_q
+ * NULL) the bf16 output projection, with the gated residual.  Arguments as
+ * flux3_block_fwd; workspace flux3_block_fp8_workspace_size bytes. */
 flux3_status flux3_block_fp8_fwd(const flux3_dims *dims, const flux3_block_weights_fp8 *w, const flux3_segments *segs,
                                  const void *x, void *x_out, int32_t n_tokens, const float *rope, void *ws,
                                  size_t ws_bytes, flux3_stream_t stream);
@@ -359,8 +365,8 @@ flux3_status flux3_block_fp8_fwd(const flux3_dims *dims, const flux3_block_weigh
  * Quantized checkpoints).  Here both operands of the input projection are NVFP4 and the
  * product runs on the block-scaled tensor cores (tcgen05 kind::mxf4nvf4):
  *   P = s_a[token] * sum_k (e2m1(a) sb_a)(e2m1(w) sb_w) * s_w[out] + b_in,
- * then the same epilogues as flux3_in_proj_fwd; the output projection stays bf16.
- * Format, per row of a bf16 [rows, k] matrix (k % 256 == 0), every step one fp32 operation
+ * then the same epilogues as flux3_in_proj_fwd; the block entry point can run the output
+ * projection the same way.  Format, per row of a bf16 [rows, k] matrix (k % 256 == 0), every step one fp32 operation
  * rounded to nearest even:
  *   g = 2688 / amax (2688 = 6 x 448; an all-zero row, or one whose g overflows fp32,
  *   gives zero codes and scales), s_row = amax / 2688;
@@ -381,9 +387,13 @@ size_t flux3_nvfp4_scale_bytes(int32_t rows, int32_t k);
 flux3_status flux3_quantize_rows_nvfp4(const void *x, int32_t rows, int32_t k, void *q, void *sf, float *scale,
                                        flux3_stream_t stream);
 
-/* One block's parameters with an NVFP4 input projection (device memory).
- *  w_in  uint8 [3D + 2F, D / 2]: W_in codes (rows Q | K | V | gate | up), w_sf their tiled
- *        block scales, s_in fp32 [3D + 2F] their row scales (flux3_quantize_rows_nvfp4).
+/* One block's parameters with NVFP4 projections (device memory).
+ *  w_in     uint8 [3D + 2F, D / 2]: W_in codes (rows Q | K | V | gate | up), w_sf their tiled
+ *           block scales, s_in fp32 [3D + 2F] their row scales (flux3_quantize_rows_nvfp4).
+ *  w_out_q  uint8 [D, (D + F) / 2]: W_out codes, w_out_sf their tiled block scales, s_out
+ *           fp32 [D] their row scales; when set, the block quantizes [attention | SwiGLU]
+ *           per token and runs the output projection on NVFP4 operands too; when NULL it
+ *           runs in bf16 on w_out.
  *  Other fields as flux3_block_weights. */
 typedef struct flux3_block_weights_nvfp4 {
     const void *w_in;
@@ -394,6 +404,9 @@ typedef struct flux3_block_weights_nvfp4 {
     const float *k_norm;
     const void *w_out;
     const float *b_out;
+    const void *w_out_q;
+    const void *w_out_sf;
+    const float *s_out;
 } flux3_block_weights_nvfp4;
 
 /* flux3_in_proj_fwd (one weight set) on NVFP4 operands: a4 uint8 [N, D / 2] codes of the
@@ -405,10 +418,11 @@ flux3_status flux3_in_proj_nvfp4_fwd(const flux3_dims *dims, const flux3_block_w
 
 size_t flux3_block_nvfp4_workspace_size(const flux3_dims *dims, int32_t n_tokens);
 
-/* The joint block (stage 2) with the NVFP4 input projection: LayerNorm + modulation (bf16),
- * NVFP4 row quantization, the block-scaled input projection with its epilogues, attention,
- * bf16 output projection with the gated residual.  Arguments as flux3_block_fwd; workspace
- * flux3_block_nvfp4_workspace_size bytes. */
+/* The joint block (stage 2) with NVFP4 projections: LayerNorm + modulation (bf16), NVFP4
+ * row quantization, the block-scaled input projection with its epilogues, attention, then
+ * (w_out_q set) NVFP4 row quantization of [attention | SwiGLU] and the block-scaled output
+ * projection, or (w_out_q NULL) the bf16 output projection, with the gated residual.
+ * Arguments as flux3_block_fwd; workspace flux3_block_nvfp4_workspace_size bytes. */
 flux3_status flux3_block_nvfp4_fwd(const flux3_dims *dims, const flux3_block_weights_nvfp4 *w,
                                    const flux3_segments *segs, const void *x, void *x_out, int32_t n_tokens,
                                    const float *rope, void *ws, size_t ws_bytes, flux3_stream_t stream);

@@ -98,3 +98,24 @@ def test_block_fp8_full_size_sampled():
     ref = O.block_forward_rows(synth.as_f64(case.x), [oracle_weights(case.weights[0])], case.seg_off,
                                synth.as_f64(case.mod), ang, d.heads, rows, rounding="bf16", fp8_in_proj=True)
     assert_close("x_out (rows, fp8 projection)", f64(out[rows]), ref["x_out"])
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_block_fp8_both_projections(cfg):
+    """Both projections on row-wise e4m3 operands: tiny (every row) and the full 4,256-token
+    block (sampled rows)."""
+    case = synth.config(cfg, bias=cfg == 0)
+    d = case.dims
+    w = B.Fp8Weights(DevWeights(case.weights[0], bias=cfg == 0), quantize_out=True)
+    rope = B.rope_build(d, case.pos.cuda())
+    out = B.block_fp8_fwd(d, w, case.seg_off, case.mod.cuda(), case.x.cuda(), rope)
+    torch.cuda.synchronize()
+    ang = O.rope_angles(case.pos.numpy(), d.rope_theta)
+    args = (synth.as_f64(case.x), [oracle_weights(case.weights[0])], case.seg_off, synth.as_f64(case.mod), ang, d.heads)
+    kw = dict(rounding="bf16", fp8_in_proj=True, out_proj_quant="fp8")
+    if cfg == 0:
+        assert_close("x_out (fp8 projections)", f64(out), O.block_forward(*args, **kw).x_out)
+    else:
+        rows = TP._sample_rows(case)
+        ref = O.block_forward_rows(*args, rows, **kw)
+        assert_close("x_out (rows, fp8 projections)", f64(out[rows]), ref["x_out"])
