@@ -73,8 +73,8 @@ def block_flops(D, F, n):
 # DRAM traffic of one in_proj launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
 # ncu capture summarised in profiles/joint_block_4256_ncu_full.md; reported only while the
 # kernel sources are the ones that capture measured.
-IN_PROJ_TRAFFIC_BYTES = (203.328000 + 140.620800) * 1e6
-IN_PROJ_SOURCES = {"gemm.cuh": "d9922c202fae3d42", "sm103.cuh": "505ea2de50cad3d3", "flux3.cu": "ff0901d8a9fae7eb"}
+IN_PROJ_TRAFFIC_BYTES = (201.138432 + 140.202240) * 1e6
+IN_PROJ_SOURCES = {"gemm.cuh": "b2571096384aaa0a", "sm103.cuh": "86ccb8d589deb628", "flux3.cu": "a9964237d87c6d29"}
 
 
 def in_proj_traffic():
