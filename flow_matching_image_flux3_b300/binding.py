@@ -108,6 +108,9 @@ def _load() -> ctypes.CDLL:
                                         c_i32, c_vp, c_vp, c_size, c_vp]),
         "flux3_sample_fwd": (c_i32, [P(flux3_dims), P(flux3_dit_weights), P(flux3_sample_args), c_vp, c_vp, c_size,
                                      c_vp]),
+        "flux3_block_bwd_workspace_size": (c_size, [P(flux3_dims), c_i32]),
+        "flux3_block_bwd": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp, c_vp, c_i32,
+                                    c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
         "flux3_nvfp4_scale_bytes": (c_size, [c_i32, c_i32]),
         "flux3_quantize_rows_nvfp4": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
         "flux3_in_proj_nvfp4_fwd": (c_i32, [P(flux3_dims), P(flux3_block_weights_nvfp4), c_vp, c_vp, c_vp, c_i32, c_vp,
@@ -139,6 +142,7 @@ EXPORTED = [
     "flux3_sample_fwd", "flux3_quantize_rows_fp8", "flux3_in_proj_fp8_fwd", "flux3_block_fp8_workspace_size",
     "flux3_block_fp8_fwd", "flux3_selftest_timeout", "flux3_nvfp4_scale_bytes", "flux3_quantize_rows_nvfp4",
     "flux3_in_proj_nvfp4_fwd", "flux3_block_nvfp4_workspace_size", "flux3_block_nvfp4_fwd",
+    "flux3_block_bwd_workspace_size", "flux3_block_bwd",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -510,6 +514,35 @@ def block_fp8_fwd(dims, weights: Fp8Weights, seg_off: Sequence[int], mod: torch.
                                                           _ptr(rope, torch.float32), _ptr(ws), ws.numel(),
                                                           _stream(stream)))
     return x_out
+
+
+def block_bwd_workspace_size(dims, n: int) -> int:
+    d = make_dims(dims)
+    return int(lib.flux3_block_bwd_workspace_size(ctypes.byref(d), n))
+
+
+def block_bwd(dims, weights, seg_off: Sequence[int], mod: torch.Tensor, x: torch.Tensor, rope: torch.Tensor,
+              dxo: torch.Tensor, ws: Optional[torch.Tensor] = None, out: Optional[dict] = None, stream=None) -> dict:
+    """Gradients of the joint block (flux3_block_bwd) for the output gradient dxo (fp32
+    [N, D]): a dict of dx, dw_in, db_in, dq_norm, dk_norm, dw_out, db_out, dmod (fp32)."""
+    n, D = x.shape
+    F = dims.ffn_hidden
+    dev = x.device
+    if out is None:
+        out = {"dx": torch.empty(n, D, device=dev), "dw_in": torch.empty(3 * D + 2 * F, D, device=dev),
+               "db_in": torch.empty(3 * D + 2 * F, device=dev), "dq_norm": torch.empty(128, device=dev),
+               "dk_norm": torch.empty(128, device=dev), "dw_out": torch.empty(D, D + F, device=dev),
+               "db_out": torch.empty(D, device=dev), "dmod": torch.empty(len(seg_off) - 1, 3, D, device=dev)}
+    ws = ws if ws is not None else workspace(block_bwd_workspace_size(dims, n), dev)
+    d, s = make_dims(dims), Segments(seg_off, mod)
+    w = block_weights(weights)
+    f = lambda k: _ptr(out[k], torch.float32)
+    _check("flux3_block_bwd", lib.flux3_block_bwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(s.s),
+                                                  _ptr(x, torch.bfloat16), _ptr(rope, torch.float32),
+                                                  _ptr(dxo, torch.float32), n, f("dx"), f("dw_in"), f("db_in"),
+                                                  f("dq_norm"), f("dk_norm"), f("dw_out"), f("db_out"), f("dmod"),
+                                                  _ptr(ws), ws.numel(), _stream(stream)))
+    return out
 
 
 def nvfp4_scale_bytes(rows: int, k: int) -> int:

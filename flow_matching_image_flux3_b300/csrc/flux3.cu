@@ -17,6 +17,7 @@
 #include "gemm.cuh"
 #include "gemm_nvf4.cuh"
 #include "attention.cuh"
+#include "bwd.cuh"
 
 using namespace f3;
 
@@ -551,6 +552,7 @@ flux3_status run_final(const flux3_dims* d, const void* w_final, const float* b_
     P.width = D;
     P.out = out;
     P.ld_out = out_ch;
+    P.n_cols = out_ch;
     return launch_gemm<128, EPI_F32, 1>(P, st, FLUX3_KERNEL_FINAL);
 }
 
@@ -570,7 +572,46 @@ flux3_status run_linear(const flux3_dims* d, const void* x, int rows, int k, con
     P.width = D;
     P.out_bf = static_cast<__nv_bfloat16*>(out);
     P.ld_out = ld_out;
+    P.n_cols = D;
     return launch_gemm<256, EPI_BF16, 1>(P, st, FLUX3_KERNEL_LINEAR);
+}
+
+// C[M, N] = A[M, K] B[N, K]^T (+ bias): bf16 K-major operands with row strides in elements
+// (multiples of 8), ragged M, N and K (the tensor maps read zeros past K and past the B
+// rows; the epilogue stores only the N columns); C fp32 or bf16 with row stride ldc.
+flux3_status run_gemm_plain(const void* A, int lda, const void* B, int ldb, int M, int N, int K, const float* bias,
+                            void* C, int ldc, bool c_bf16, cudaStream_t st) {
+    if (M == 0 || N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    if (!tmap_2d(&P.tm_a, A, K, M, (uint64_t)lda * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_2d(&P.tm_b[0], B, K, N, (uint64_t)ldb * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    P.ew[0] = {bias, nullptr, nullptr};
+    const int32_t off[2] = {0, M};
+    fill_groups(P, off, 1, 1, M, 1);
+    P.k_blocks = (K + GEMM_BK - 1) / GEMM_BK;
+    P.n_cols = N;
+    P.ld_out = ldc;
+    if (c_bf16) P.out_bf = static_cast<__nv_bfloat16*>(C);
+    else P.out = static_cast<float*>(C);
+    if (N <= 128) {
+        P.n_tiles = 1;
+        return c_bf16 ? launch_gemm<128, EPI_BF16, 1>(P, st, FLUX3_KERNEL_BWD_GEMM)
+                      : launch_gemm<128, EPI_F32, 1>(P, st, FLUX3_KERNEL_BWD_GEMM);
+    }
+    P.n_tiles = (N + 255) / 256;
+    return c_bf16 ? launch_gemm<256, EPI_BF16, 1>(P, st, FLUX3_KERNEL_BWD_GEMM)
+                  : launch_gemm<256, EPI_F32, 1>(P, st, FLUX3_KERNEL_BWD_GEMM);
+}
+
+// dst [cols, ld_dst] = src [rows, cols]^T (bf16)
+flux3_status run_transpose(const void* src, int rows, int cols, int ld_src, void* dst, int ld_dst, cudaStream_t st) {
+    if (rows == 0 || cols == 0) return FLUX3_OK;
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    transpose_bf16_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32)), dim3(32, 8), 0, st>>>(
+        static_cast<const __nv_bfloat16*>(src), rows, cols, ld_src, static_cast<__nv_bfloat16*>(dst), ld_dst);
+    prof_after(st);
+    return launch_status();
 }
 
 flux3_status run_cfg_euler(float* latent, const float* vp, const float* vn, long long n, float s, float dt,
@@ -1230,6 +1271,179 @@ flux3_status flux3_block_nvfp4_fwd(const flux3_dims* dims, const flux3_block_wei
     }
     const flux3_block_weights wo{nullptr, nullptr, nullptr, nullptr, w->w_out, w->b_out};
     return run_out_proj(dims, &wo, 1, segs, b.y, x, x_out, N, st);
+}
+
+// ---------------------------------------------------------------- the joint block's backward
+namespace {
+struct BwdWs {
+    BlockWs f;                      // the forward pass recomputed: a, q, k, V^T, [O | act]
+    __nv_bfloat16 *p, *dy, *dyT, *woT, *wiT, *dycat, *ycatT, *pr, *prT, *ds, *doT, *kT, *qT, *dp, *dpT, *aT;
+    float *yout, *s, *dq, *dk, *dv, *da;
+    float2* stats;
+    int ldn;  // row stride of the [., N] buffers (N rounded up to 8)
+    size_t bytes;
+};
+BwdWs bwd_ws_layout(const flux3_dims* d, int N, uint8_t* base) {
+    BwdWs w;
+    w.f = block_ws_layout(d, N, base);
+    const size_t D = d->width, F = d->ffn_hidden, n_in = 3 * D + 2 * F;
+    w.ldn = (N + 7) & ~7;
+    const size_t ldn = w.ldn;
+    size_t off = w.f.bytes;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? base + off : nullptr;
+        off += up256(bytes);
+        return p;
+    };
+    auto bf = [&](size_t elems) { return reinterpret_cast<__nv_bfloat16*>(take(elems * 2)); };
+    auto f32 = [&](size_t elems) { return reinterpret_cast<float*>(take(elems * 4)); };
+    w.p = bf((size_t)N * n_in);
+    w.yout = f32((size_t)N * D);
+    w.dy = bf((size_t)N * D);
+    w.dyT = bf(D * ldn);
+    w.woT = bf((D + F) * D);
+    w.wiT = bf(D * n_in);
+    w.dycat = bf((size_t)N * (D + F));
+    w.ycatT = bf((D + F) * ldn);
+    w.s = f32((size_t)N * ldn);
+    w.pr = bf((size_t)N * ldn);
+    w.prT = bf((size_t)N * ldn);
+    w.ds = bf((size_t)N * ldn);
+    w.doT = bf(128 * ldn);
+    w.kT = bf(128 * ldn);
+    w.qT = bf(128 * ldn);
+    w.dq = f32((size_t)N * D);
+    w.dk = f32((size_t)N * D);
+    w.dv = f32((size_t)N * D);
+    w.dp = bf((size_t)N * n_in);
+    w.dpT = bf(n_in * ldn);
+    w.aT = bf(D * ldn);
+    w.da = f32((size_t)N * D);
+    w.stats = reinterpret_cast<float2*>(take((size_t)N * 8));
+    w.bytes = off;
+    return w;
+}
+}  // namespace
+
+size_t flux3_block_bwd_workspace_size(const flux3_dims* dims, int32_t n_tokens) {
+    if (check_dims(dims) != FLUX3_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
+    return bwd_ws_layout(dims, n_tokens, nullptr).bytes;
+}
+
+flux3_status flux3_block_bwd(const flux3_dims* dims, const flux3_block_weights* w, const flux3_segments* segs,
+                             const void* x, const float* rope, const float* dxo, int32_t n_tokens, float* dx, float* dw_in,
+                             float* db_in, float* dq_norm, float* dk_norm, float* dw_out, float* db_out, float* dmod,
+                             void* ws, size_t ws_bytes, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    const int N = n_tokens;
+    if (N < 0 || N > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, N, true)) != FLUX3_OK) return s;
+    if ((s = check_weights(w, 1, true, true)) != FLUX3_OK) return s;
+    if (dims->width % 256 != 0) return FLUX3_ERR_UNSUPPORTED;
+    if (N == 0) return FLUX3_OK;
+    if (!x || !rope || !dxo || !dx || !dw_in || !db_in || !dq_norm || !dk_norm || !dw_out || !db_out || !dmod)
+        return FLUX3_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(rope) || !al16(dxo) || !al16(dx) || !al16(dw_in) || !al16(dw_out)) return FLUX3_ERR_INVALID_ARG;
+    if (!ws || !al256(ws) || ws_bytes < flux3_block_bwd_workspace_size(dims, N)) return FLUX3_ERR_WORKSPACE;
+    if (!have_encode()) return FLUX3_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const BwdWs b = bwd_ws_layout(dims, N, static_cast<uint8_t*>(ws));
+    const int D = dims->width, F = dims->ffn_hidden, H = dims->heads, n_in = 3 * D + 2 * F, ldy = D + F, ldn = b.ldn;
+    const SegOffsets so = seg_table(segs->seg_off, segs->n_seg);
+    const int n_seg = segs->n_seg;
+    const float sc = (float)(1.0 / std::sqrt(128.0));
+    // outputs that accumulate
+    if (cudaMemsetAsync(db_in, 0, (size_t)n_in * 4, st) != cudaSuccess || cudaMemsetAsync(dq_norm, 0, 128 * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(dk_norm, 0, 128 * 4, st) != cudaSuccess || cudaMemsetAsync(db_out, 0, (size_t)D * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(dmod, 0, (size_t)n_seg * 3 * D * 4, st) != cudaSuccess)
+        return FLUX3_ERR_CUDA;
+
+    // ---- the forward pass again: a, q, k, V^T, [O | act], the projections P and y
+    if ((s = run_adaln(dims, segs->mod, so, x, N, b.f.a, st)) != FLUX3_OK) return s;
+    if ((s = run_in_proj(dims, w, 1, segs, b.f.a, N, rope, b.f.q, b.f.k, b.f.vt, b.f.ld_vt, b.f.y, st)) != FLUX3_OK) return s;
+    const int32_t full[2] = {0, N};
+    if ((s = run_attn(dims, b.f.q, b.f.k, b.f.vt, b.f.ld_vt, N, full, 1, b.f.y, ldy, false, st)) != FLUX3_OK) return s;
+    if ((s = run_gemm_plain(b.f.a, D, w->w_in, D, N, n_in, D, w->b_in, b.p, n_in, true, st)) != FLUX3_OK) return s;
+    if ((s = run_gemm_plain(b.f.y, ldy, w->w_out, ldy, N, D, ldy, w->b_out, b.yout, D, false, st)) != FLUX3_OK) return s;
+
+    // ---- x' = x + gate y
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    bwd_gate_kernel<<<dim3((unsigned)((N + BWD_ROWS - 1) / BWD_ROWS), (unsigned)(D / 256)), 256, 0, st>>>(
+        dxo, b.yout, N, D, segs->mod, so, b.dy, dmod, db_out);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    // ---- y = [O | act] W_out^T + b_out
+    if ((s = run_transpose(w->w_out, D, ldy, ldy, b.woT, D, st)) != FLUX3_OK) return s;
+    if ((s = run_gemm_plain(b.dy, D, b.woT, D, N, ldy, D, nullptr, b.dycat, ldy, true, st)) != FLUX3_OK) return s;
+    if ((s = run_transpose(b.dy, N, D, D, b.dyT, ldn, st)) != FLUX3_OK) return s;
+    if ((s = run_transpose(b.f.y, N, ldy, ldy, b.ycatT, ldn, st)) != FLUX3_OK) return s;
+    if ((s = run_gemm_plain(b.dyT, ldn, b.ycatT, ldn, D, ldy, N, nullptr, dw_out, ldy, false, st)) != FLUX3_OK) return s;
+    // ---- act = silu(G) U
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    bwd_swiglu_kernel<<<(unsigned)(8 * sm_count()), 256, 0, st>>>(b.dycat, b.p, N, D, F, b.dp);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    // ---- attention, one head at a time with the score matrix in HBM
+    for (int h = 0; h < H; ++h) {
+        const __nv_bfloat16* qh = b.f.q + (size_t)h * N * 128;
+        const __nv_bfloat16* kh = b.f.k + (size_t)h * N * 128;
+        const __nv_bfloat16* doh = b.dycat + (size_t)h * 128;     // row stride ldy
+        const __nv_bfloat16* oh = b.f.y + (size_t)h * 128;        // row stride ldy
+        const __nv_bfloat16* vh = b.p + 2 * D + (size_t)h * 128;  // row stride n_in
+        if ((s = run_gemm_plain(qh, 128, kh, 128, N, N, 128, nullptr, b.s, ldn, false, st)) != FLUX3_OK) return s;
+        prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+        softmax_rows_kernel<<<(unsigned)N, 256, 0, st>>>(b.s, N, ldn, sc, b.pr, ldn);
+        prof_after(st);
+        if ((s = launch_status()) != FLUX3_OK) return s;
+        if ((s = run_transpose(b.pr, N, N, ldn, b.prT, ldn, st)) != FLUX3_OK) return s;
+        if ((s = run_transpose(doh, N, 128, ldy, b.doT, ldn, st)) != FLUX3_OK) return s;
+        // dV = P^T dO
+        if ((s = run_gemm_plain(b.prT, ldn, b.doT, ldn, N, 128, N, nullptr, b.dv + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+            return s;
+        // dP = dO V^T, then dS = scale P (dP - rowsum(dO O))
+        if ((s = run_gemm_plain(doh, ldy, vh, n_in, N, N, 128, nullptr, b.s, ldn, false, st)) != FLUX3_OK) return s;
+        prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+        attn_ds_kernel<<<(unsigned)N, 256, 0, st>>>(b.s, ldn, b.pr, ldn, doh, ldy, oh, ldy, N, sc, b.ds, ldn);
+        prof_after(st);
+        if ((s = launch_status()) != FLUX3_OK) return s;
+        // dQ = dS K, dK = dS^T Q
+        if ((s = run_transpose(kh, N, 128, 128, b.kT, ldn, st)) != FLUX3_OK) return s;
+        if ((s = run_gemm_plain(b.ds, ldn, b.kT, ldn, N, 128, N, nullptr, b.dq + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+            return s;
+        if ((s = run_transpose(b.ds, N, N, ldn, b.prT, ldn, st)) != FLUX3_OK) return s;
+        if ((s = run_transpose(qh, N, 128, 128, b.qT, ldn, st)) != FLUX3_OK) return s;
+        if ((s = run_gemm_plain(b.prT, ldn, b.qT, ldn, N, 128, N, nullptr, b.dk + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+            return s;
+    }
+    // ---- RoPE, QK RMSNorm and the V columns of dP; then P = a W_in^T + b_in
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    bwd_qk_kernel<<<(unsigned)(4 * sm_count()), 256, 0, st>>>(b.dq, b.dk, b.dv, b.p, reinterpret_cast<const float2*>(rope),
+                                                             w->q_norm, w->k_norm, dims->rms_eps, N, H, D, F, b.dp, dq_norm,
+                                                             dk_norm);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    colsum_bf16_kernel<<<dim3((unsigned)((n_in + 255) / 256), (unsigned)((N + 63) / 64)), 256, 0, st>>>(b.dp, N, n_in, n_in,
+                                                                                                    db_in);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    if ((s = run_transpose(w->w_in, n_in, D, D, b.wiT, n_in, st)) != FLUX3_OK) return s;
+    if ((s = run_gemm_plain(b.dp, n_in, b.wiT, n_in, N, D, n_in, nullptr, b.da, D, false, st)) != FLUX3_OK) return s;
+    if ((s = run_transpose(b.dp, N, n_in, n_in, b.dpT, ldn, st)) != FLUX3_OK) return s;
+    if ((s = run_transpose(b.f.a, N, D, D, b.aT, ldn, st)) != FLUX3_OK) return s;
+    if ((s = run_gemm_plain(b.dpT, ldn, b.aT, ldn, n_in, D, N, nullptr, dw_in, D, false, st)) != FLUX3_OK) return s;
+    // ---- LayerNorm + modulation
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    bwd_ln_kernel<<<(unsigned)((N + 7) / 8), 256, 0, st>>>(b.da, static_cast<const __nv_bfloat16*>(x), dxo, segs->mod, so,
+                                                           dims->ln_eps, N, D, dx, b.stats);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    bwd_mod_kernel<<<dim3((unsigned)((N + BWD_ROWS - 1) / BWD_ROWS), (unsigned)(D / 256)), 256, 0, st>>>(
+        b.da, static_cast<const __nv_bfloat16*>(x), b.stats, N, D, so, dmod);
+    prof_after(st);
+    return launch_status();
 }
 
 flux3_status flux3_device_error(uint32_t* flags, int32_t reset) {

@@ -63,6 +63,7 @@ struct GemmParams {
     float* out;
     __nv_bfloat16* out_bf;
     int ld_out;
+    int n_cols;  // columns of the output: a tile's columns at or past it are not stored
 };
 
 template <int BN>
@@ -287,19 +288,25 @@ F3_DEV void epi_f32(const GemmParams& p, const EpiWeights& w, int n, uint32_t ta
         uint32_t t[32];
         tmem_ld32(tacc + c * 32, t);
         tmem_ld_wait();
-        if (!valid) continue;
         const int col = n * BN + c * 32;
+        if (!valid || col >= p.n_cols) continue;
         float a[32];
         unpack32(t, a);
-        if (w.bias) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
-        }
         float* dst = p.out + (size_t)r * p.ld_out + col;
+        if (col + 32 <= p.n_cols) {
+            if (w.bias) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            st_global_v4(dst + 4 * i, __float_as_uint(a[4 * i]), __float_as_uint(a[4 * i + 1]), __float_as_uint(a[4 * i + 2]),
-                         __float_as_uint(a[4 * i + 3]));
+                for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st_global_v4(dst + 4 * i, __float_as_uint(a[4 * i]), __float_as_uint(a[4 * i + 1]),
+                             __float_as_uint(a[4 * i + 2]), __float_as_uint(a[4 * i + 3]));
+        } else {  // the ragged last columns
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col + i < p.n_cols) dst[i] = a[i] + (w.bias ? __ldg(w.bias + col + i) : 0.f);
+        }
     }
 }
 
@@ -310,19 +317,25 @@ F3_DEV void epi_bf16(const GemmParams& p, const EpiWeights& w, int n, uint32_t t
         uint32_t t[32];
         tmem_ld32(tacc + c * 32, t);
         tmem_ld_wait();
-        if (!valid) continue;
         const int col = n * BN + c * 32;
+        if (!valid || col >= p.n_cols) continue;
         float a[32];
         unpack32(t, a);
-        if (w.bias) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
-        }
         __nv_bfloat16* dst = p.out_bf + (size_t)r * p.ld_out + col;
+        if (col + 32 <= p.n_cols) {
+            if (w.bias) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            st_global_v4(dst + 8 * i, pack_bf16(a[8 * i], a[8 * i + 1]), pack_bf16(a[8 * i + 2], a[8 * i + 3]),
-                         pack_bf16(a[8 * i + 4], a[8 * i + 5]), pack_bf16(a[8 * i + 6], a[8 * i + 7]));
+                for (int i = 0; i < 32; ++i) a[i] += __ldg(w.bias + col + i);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                st_global_v4(dst + 8 * i, pack_bf16(a[8 * i], a[8 * i + 1]), pack_bf16(a[8 * i + 2], a[8 * i + 3]),
+                             pack_bf16(a[8 * i + 4], a[8 * i + 5]), pack_bf16(a[8 * i + 6], a[8 * i + 7]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col + i < p.n_cols) dst[i] = __float2bfloat16_rn(a[i] + (w.bias ? __ldg(w.bias + col + i) : 0.f));
+        }
     }
 }
 

@@ -427,6 +427,25 @@ flux3_status flux3_block_nvfp4_fwd(const flux3_dims *dims, const flux3_block_wei
                                    const flux3_segments *segs, const void *x, void *x_out, int32_t n_tokens,
                                    const float *rope, void *ws, size_t ws_bytes, flux3_stream_t stream);
 
+/* ---- the joint block's backward pass (fine-tuning the base checkpoint: "FLUX 3 Image
+ * Klein" Miles page, section 1; the block of "Welcome FLUX.3 Image Klein in Diffusers",
+ * "How it works").  For a loss whose gradient with respect to the block output x' is dxo,
+ * the gradients of the block input and of every parameter of flux3_block_fwd:
+ *   dx      fp32 [N, D]          dw_in  fp32 [3D + 2F, D]   db_in  fp32 [3D + 2F]
+ *   dq_norm fp32 [128]           dk_norm fp32 [128]         dw_out fp32 [D, D + F]
+ *   db_out  fp32 [D]             dmod   fp32 [n_seg][3][D]  (shift, scale, gate, each summed
+ *                                                            over its stream's rows)
+ * The forward pass is recomputed inside (no saved activations); attention's score and
+ * probability matrices are materialized in the workspace one head at a time.  Arguments x,
+ * rope, segs, w as flux3_block_fwd (w's biases may be NULL: their gradients are still
+ * written); dxo fp32 [N, D].  All outputs are overwritten; workspace
+ * flux3_block_bwd_workspace_size bytes (about 1.6 GB at N = 4,256 and width 3072). */
+size_t flux3_block_bwd_workspace_size(const flux3_dims *dims, int32_t n_tokens);
+flux3_status flux3_block_bwd(const flux3_dims *dims, const flux3_block_weights *w, const flux3_segments *segs,
+                             const void *x, const float *rope, const float *dxo, int32_t n_tokens, float *dx,
+                             float *dw_in, float *db_in, float *dq_norm, float *dk_norm, float *dw_out, float *db_out,
+                             float *dmod, void *ws, size_t ws_bytes, flux3_stream_t stream);
+
 /* ---- flux3_block_fwd without a caller-provided workspace.
  * This entry point has no counterpart in the model description; it is a service for
  * callers that cannot allocate device memory: for example a host program that hands all
@@ -473,7 +492,7 @@ enum {
     FLUX3_KERNEL_ROPE = 1, FLUX3_KERNEL_ADALN = 2, FLUX3_KERNEL_IN_PROJ = 3,
     FLUX3_KERNEL_ATTN = 4, FLUX3_KERNEL_OUT_PROJ = 5, FLUX3_KERNEL_FINAL = 6,
     FLUX3_KERNEL_EULER = 7, FLUX3_KERNEL_ATTN_F32 = 8, FLUX3_KERNEL_LINEAR = 9, FLUX3_KERNEL_CFG_EULER = 10,
-    FLUX3_KERNEL_TO_BF16 = 11, FLUX3_KERNEL_QUANTIZE = 12
+    FLUX3_KERNEL_TO_BF16 = 11, FLUX3_KERNEL_QUANTIZE = 12, FLUX3_KERNEL_BWD_GEMM = 13, FLUX3_KERNEL_BWD_ELEM = 14
 };
 flux3_status flux3_profile_begin(int32_t capacity);
 flux3_status flux3_profile_end(float *ms, int32_t *kinds, int32_t capacity, int32_t *n);

@@ -88,13 +88,15 @@ def block_backward(x: np.ndarray, w: Weights, seg_off: Sequence[int], mod: np.nd
     q = rope_rotate(qn, angles)
     k = rope_rotate(kn, angles)
     sc = 1.0 / math.sqrt(d)
-    probs = np.empty((H, n, n))
-    o = np.empty((n, H, d))
-    for h in range(H):
+
+    def probs(h):
         s = q[:, h] @ k[:, h].T * sc
         s = np.exp(s - s.max(axis=1, keepdims=True))
-        probs[h] = s / s.sum(axis=1, keepdims=True)
-        o[:, h] = probs[h] @ v[:, h]
+        return s / s.sum(axis=1, keepdims=True)
+
+    o = np.empty((n, H, d))
+    for h in range(H):
+        o[:, h] = probs(h) @ v[:, h]
     sig = 1.0 / (1.0 + np.exp(-g))
     act = g * sig * u
     ycat = np.concatenate([o.reshape(n, D), act], axis=1)
@@ -116,7 +118,7 @@ def block_backward(x: np.ndarray, w: Weights, seg_off: Sequence[int], mod: np.nd
     du = dact * g * sig
     dq = np.empty((n, H, d)); dk = np.empty((n, H, d)); dv = np.empty((n, H, d))
     for h in range(H):
-        pr = probs[h]
+        pr = probs(h)
         dv[:, h] = pr.T @ do[:, h]
         dpr = do[:, h] @ v[:, h].T
         delta = (do[:, h] * o[:, h]).sum(axis=1, keepdims=True)
