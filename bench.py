@@ -37,14 +37,14 @@ def parse():
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=["joint", "joint_fp8", "joint_nvfp4", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
+    p.add_argument("--workload", choices=["joint", "joint_fp8", "joint_nvfp4", "joint_bwd", "stage1", "joint_ref", "refs10", "refs10_s1", "dit",
                                           "loop", "loop_ref"],
                    default="joint",
                    help="joint: the headline 4,256-token joint block.  The others print one line each for "
                         "the other workloads: stage1 (three streams 4096|4096|240, own weights), joint_ref "
                         "(4096+4096+160 tokens), refs10 / refs10_s1 (image + ten references + text = 45,216 "
                         "tokens, joint / per-stream block), joint_fp8 / joint_nvfp4 (the 4,256-token joint block with the "
-                        "e4m3 / NVFP4 input projection), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
+                        "e4m3 / NVFP4 projections), joint_bwd (its backward pass), dit (5 stage-1 + 28 joint blocks + output layer, one forward), "
                         "loop (the 50-step guided sampling loop through flux3_sample_fwd, eager without and with the "
                         "context cache, and as a CUDA graph), loop_ref (the same with one 1024x1024 reference)")
     args = p.parse_args()
@@ -58,7 +58,7 @@ def parse():
 
 # Default (timed steps, warm-up steps) per workload: about half a minute of timed work each
 # (a sampling-loop step is one whole 50-step image, ~3.5 s; ~8 s with a reference).
-DEFAULT_STEPS = {"joint": (1000, 20), "joint_fp8": (1000, 20), "joint_nvfp4": (1000, 20), "stage1": (1000, 20), "joint_ref": (1000, 20),
+DEFAULT_STEPS = {"joint": (1000, 20), "joint_fp8": (1000, 20), "joint_nvfp4": (1000, 20), "joint_bwd": (50, 3), "stage1": (1000, 20), "joint_ref": (1000, 20),
                  "refs10": (100, 5), "refs10_s1": (100, 5), "dit": (200, 5), "loop": (2, 1),
                  "loop_ref": (1, 1)}
 
@@ -449,7 +449,44 @@ def run_workload(args):
     stream = torch.cuda.current_stream()
     out = {"impl": "ours", "workload": args.workload, "n_gpus": 1, "data": "synthetic", "dtype": "bf16",
            "higher_is_better": True, "unit": "tokens/s"}
-    if args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1", "joint_fp8", "joint_nvfp4"):
+    if args.workload == "joint_bwd":
+        # the joint block's backward pass at 4,256 tokens (forward recomputed inside), for a
+        # random output gradient; weights and input of the headline workload
+        case = synth.config(1)
+        d, N = case.dims, case.n
+        D, F = d.width, d.ffn_hidden
+
+        class DWb:
+            def __init__(self, w):
+                self.w_in, self.b_in = w.w_in.to(dev), None
+                self.q_norm, self.k_norm = w.q_norm.to(dev), w.k_norm.to(dev)
+                self.w_out, self.b_out = w.w_out.to(dev), None
+        wb = DWb(case.weights[0])
+        x, mod, pos = case.x.to(dev), case.mod.to(dev), case.pos.to(dev)
+        rope = B.rope_build(d, pos)
+        dxo = torch.randn(N, D, generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+        wsp = B.workspace(B.block_bwd_workspace_size(d, N), dev)
+        grads = B.block_bwd(d, wb, case.seg_off, mod, x, rope, dxo, ws=wsp, stream=stream)
+
+        def step():
+            B.block_bwd(d, wb, case.seg_off, mod, x, rope, dxo, ws=wsp, out=grads, stream=stream)
+        ms = _timed(step, args.steps, args.warmup, stream)
+        g1, at, g2 = block_flops(D, F, N)
+        bwd_flops = 2 * (g1 + g2) + 2.5 * at          # dX and dW of both projections, attention backward
+        executed = bwd_flops + (g1 + at + g2) + (g1 + g2) + at / 2   # + the forward, P and y again, QK^T again
+        with B.Profile(capacity=4096) as prof:
+            for _ in range(3):
+                step()
+        per = {}
+        for name, t in prof.records:
+            per.setdefault(name, []).append(t)
+        out.update({"metric": "joint block backward tokens/s", "value": N / (ms / 1e3), "ms_per_step": ms,
+                    "tflops": bwd_flops / (ms / 1e3) / 1e12, "tflops_executed": executed / (ms / 1e3) / 1e12,
+                    "steps": args.steps, "warmup": args.warmup,
+                    "config": {"tokens": N, "flops_backward": bwd_flops, "flops_executed": executed},
+                    "kernels_ms_per_step": {k: sum(v) / 3 for k, v in per.items()},
+                    "kernels_launches_per_step": {k: len(v) // 3 for k, v in per.items()}})
+    elif args.workload in ("stage1", "joint_ref", "refs10", "refs10_s1", "joint_fp8", "joint_nvfp4"):
         if args.workload in ("joint_fp8", "joint_nvfp4"):
             case = synth.config(1)
         elif args.workload.startswith("refs10"):

@@ -20,7 +20,7 @@ c_i32, c_f32, c_vp, c_size = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ct
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 MAX_SEGMENTS = 16
 KERNEL_NAMES = {1: "rope", 2: "adaln", 3: "in_proj", 4: "attn", 5: "out_proj", 6: "final", 7: "euler", 8: "attn_f32",
-                9: "linear", 10: "cfg_euler", 11: "to_bf16", 12: "quantize"}
+                9: "linear", 10: "cfg_euler", 11: "to_bf16", 12: "quantize", 13: "bwd_gemm", 14: "bwd_elem"}
 
 
 class flux3_dims(ctypes.Structure):
