@@ -37,6 +37,7 @@ struct AttnParams {
     __nv_bfloat16* out;
     int ld_out;
     float scale_log2;  // log2(e) / sqrt(128)
+    float* lse;        // optional [heads][n_tokens]: each row's log2-sum-exp2 of scale_log2 * scores
 };
 
 // ------------------------------------------------------------------ softmax arithmetic
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) attn_tcgen05_kernel(const __gr
             const int qrow = q0 + 128 * t + row;
             const bool valid = qrow < seg_hi;
             const float inv = 1.f / l;
+            if (p.lse && valid) p.lse[(size_t)head * p.n_tokens + qrow] = m + log2f(l);
             __nv_bfloat16* dst = p.out + (size_t)(valid ? qrow : 0) * p.ld_out + head * 128;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {

@@ -80,53 +80,21 @@ __global__ void bwd_swiglu_kernel(const __nv_bfloat16* __restrict__ dycat, const
     }
 }
 
-// Row softmax of scale * s (fp32 [rows, nk], row stride ld_s) -> bf16 probabilities (row
-// stride ld_p).  One CTA of 256 threads per row.
-__global__ void __launch_bounds__(256) softmax_rows_kernel(const float* __restrict__ s, int nk, int ld_s, float scale,
-                                                          __nv_bfloat16* __restrict__ prob, int ld_p) {
-    __shared__ float red[8];
-    const float* row = s + (size_t)blockIdx.x * ld_s;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float m = -INFINITY;
-    for (int j = threadIdx.x; j < nk; j += 256) m = fmaxf(m, row[j] * scale);
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    m = red[0];
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
-    __syncthreads();
-    float sum = 0.f;
-    for (int j = threadIdx.x; j < nk; j += 256) sum += __expf(row[j] * scale - m);
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) red[warp] = sum;
-    __syncthreads();
-    sum = 0.f;
-    for (int i = 0; i < 8; ++i) sum += red[i];
-    const float inv = 1.f / sum;
-    __nv_bfloat16* out = prob + (size_t)blockIdx.x * ld_p;
-    for (int j = threadIdx.x; j < nk; j += 256) out[j] = __float2bfloat16_rn(__expf(row[j] * scale - m) * inv);
-}
-
-// dS = scale * P (dP - delta), delta = sum_d dO[r][d] O[r][d] (the row's output and its
-// gradient, 128 dims).  One CTA of 256 threads per query row; bf16 out (row stride ld_ds).
-__global__ void __launch_bounds__(256) attn_ds_kernel(const float* __restrict__ dpr, int ld_dp,
-                                                     const __nv_bfloat16* __restrict__ prob, int ld_p,
-                                                     const __nv_bfloat16* __restrict__ d_o, int ld_do,
-                                                     const __nv_bfloat16* __restrict__ o, int ld_o, int nk, float scale,
-                                                     __nv_bfloat16* __restrict__ ds, int ld_ds) {
-    __shared__ float red[8];
-    const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float part = 0.f;
-    if (threadIdx.x < 128)
-        part = __bfloat162float(d_o[(size_t)r * ld_do + threadIdx.x]) * __bfloat162float(o[(size_t)r * ld_o + threadIdx.x]);
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) red[warp] = part;
-    __syncthreads();
-    float delta = 0.f;
-    for (int i = 0; i < 8; ++i) delta += red[i];
-    for (int j = threadIdx.x; j < nk; j += 256) {
-        const float pv = __bfloat162float(prob[(size_t)r * ld_p + j]);
-        ds[(size_t)r * ld_ds + j] = __float2bfloat16_rn(scale * pv * (dpr[(size_t)r * ld_dp + j] - delta));
+// delta[h][r] = sum_d dO[r][h * 128 + d] O[r][h * 128 + d]: one warp per (row, head), four
+// dims per lane.  d_o, o bf16 [N, ld] (the attention columns of d[O | act] and [O | act]).
+__global__ void __launch_bounds__(256) attn_delta_kernel(const __nv_bfloat16* __restrict__ d_o,
+                                                        const __nv_bfloat16* __restrict__ o, int ld, int N, int H,
+                                                        float* __restrict__ delta) {
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < N * H; item += warps) {
+        const int r = item / H, h = item - r * H;
+        const size_t base = (size_t)r * ld + h * 128 + 4 * lane;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = fmaf(__bfloat162float(d_o[base + i]), __bfloat162float(o[base + i]), acc);
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) delta[(size_t)h * N + r] = acc;
     }
 }
 

@@ -463,7 +463,7 @@ flux3_status run_out_proj_quant(const flux3_dims* d, bool nvfp4, const void* w_q
 }
 
 flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const void* vt, int ld_vt, int N, const int32_t* off,
-                      int n_seg, void* out, int ld_out, bool f32, cudaStream_t st) {
+                      int n_seg, void* out, int ld_out, bool f32, cudaStream_t st, float* lse = nullptr) {
     if (N == 0) return FLUX3_OK;
     const int H = d->heads;
     if (f32) {
@@ -497,6 +497,7 @@ flux3_status run_attn(const flux3_dims* d, const void* q, const void* k, const v
     P.out = static_cast<__nv_bfloat16*>(out);
     P.ld_out = ld_out;
     P.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+    P.lse = lse;
     if (pairs == 0) return FLUX3_OK;
     if (!smem_attr_once<attn_tcgen05_kernel>(ATT_SMEM_BYTES)) return FLUX3_ERR_CUDA;
     prof_before(FLUX3_KERNEL_ATTN, st);
@@ -602,6 +603,31 @@ flux3_status run_gemm_plain(const void* A, int lda, const void* B, int ldb, int 
     P.n_tiles = (N + 255) / 256;
     return c_bf16 ? launch_gemm<256, EPI_BF16, 1>(P, st, FLUX3_KERNEL_BWD_GEMM)
                   : launch_gemm<256, EPI_F32, 1>(P, st, FLUX3_KERNEL_BWD_GEMM);
+}
+
+// The attention-backward GEMMs with keys as rows and queries as columns (EPI_PROB_T: P^T
+// from k q^T and the queries' log2-sum-exp2; EPI_DS_T: dS^T from v dO^T, P^T and the
+// queries' rowsum(dO O)); bf16 C [M, N], row stride ldc.
+template <int EPI>
+flux3_status run_gemm_attn_t(const void* A, int lda, const void* B, int ldb, int M, int N, int K, const float* col_vec,
+                             const void* aux, int ld_aux, float alpha, void* C, int ldc, cudaStream_t st) {
+    if (M == 0 || N == 0) return FLUX3_OK;
+    GemmParams P;
+    std::memset(&P, 0, sizeof P);
+    if (!tmap_2d(&P.tm_a, A, K, M, (uint64_t)lda * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    if (!tmap_2d(&P.tm_b[0], B, K, N, (uint64_t)ldb * 2, 128)) return FLUX3_ERR_INVALID_ARG;
+    const int32_t off[2] = {0, M};
+    fill_groups(P, off, 1, 1, M, 1);
+    P.k_blocks = (K + GEMM_BK - 1) / GEMM_BK;
+    P.n_tiles = (N + 255) / 256;
+    P.n_cols = N;
+    P.ld_out = ldc;
+    P.out_bf = static_cast<__nv_bfloat16*>(C);
+    P.col_vec = col_vec;
+    P.aux = static_cast<const __nv_bfloat16*>(aux);
+    P.ld_aux = ld_aux;
+    P.alpha = alpha;
+    return launch_gemm<256, EPI, 1>(P, st, FLUX3_KERNEL_BWD_GEMM);
 }
 
 // dst [cols, ld_dst] = src [rows, cols]^T (bf16)
@@ -1277,8 +1303,8 @@ flux3_status flux3_block_nvfp4_fwd(const flux3_dims* dims, const flux3_block_wei
 namespace {
 struct BwdWs {
     BlockWs f;                      // the forward pass recomputed: a, q, k, V^T, [O | act]
-    __nv_bfloat16 *p, *dy, *dyT, *woT, *wiT, *dycat, *ycatT, *pr, *prT, *ds, *doT, *kT, *qT, *dp, *dpT, *aT;
-    float *yout, *s, *dq, *dk, *dv, *da;
+    __nv_bfloat16 *p, *dy, *dyT, *woT, *wiT, *dycat, *ycatT, *pT, *dsT, *dsn, *doT, *kT, *qT, *dp, *dpT, *aT;
+    float *yout, *lse, *delta, *dq, *dk, *dv, *da;
     float2* stats;
     int ldn;  // row stride of the [., N] buffers (N rounded up to 8)
     size_t bytes;
@@ -1305,10 +1331,11 @@ BwdWs bwd_ws_layout(const flux3_dims* d, int N, uint8_t* base) {
     w.wiT = bf(D * n_in);
     w.dycat = bf((size_t)N * (D + F));
     w.ycatT = bf((D + F) * ldn);
-    w.s = f32((size_t)N * ldn);
-    w.pr = bf((size_t)N * ldn);
-    w.prT = bf((size_t)N * ldn);
-    w.ds = bf((size_t)N * ldn);
+    w.lse = f32((size_t)d->heads * N);
+    w.delta = f32((size_t)d->heads * N);
+    w.pT = bf((size_t)N * ldn);
+    w.dsT = bf((size_t)N * ldn);
+    w.dsn = bf((size_t)N * ldn);
     w.doT = bf(128 * ldn);
     w.kT = bf(128 * ldn);
     w.qT = bf(128 * ldn);
@@ -1363,7 +1390,7 @@ flux3_status flux3_block_bwd(const flux3_dims* dims, const flux3_block_weights* 
     if ((s = run_adaln(dims, segs->mod, so, x, N, b.f.a, st)) != FLUX3_OK) return s;
     if ((s = run_in_proj(dims, w, 1, segs, b.f.a, N, rope, b.f.q, b.f.k, b.f.vt, b.f.ld_vt, b.f.y, st)) != FLUX3_OK) return s;
     const int32_t full[2] = {0, N};
-    if ((s = run_attn(dims, b.f.q, b.f.k, b.f.vt, b.f.ld_vt, N, full, 1, b.f.y, ldy, false, st)) != FLUX3_OK) return s;
+    if ((s = run_attn(dims, b.f.q, b.f.k, b.f.vt, b.f.ld_vt, N, full, 1, b.f.y, ldy, false, st, b.lse)) != FLUX3_OK) return s;
     if ((s = run_gemm_plain(b.f.a, D, w->w_in, D, N, n_in, D, w->b_in, b.p, n_in, true, st)) != FLUX3_OK) return s;
     if ((s = run_gemm_plain(b.f.y, ldy, w->w_out, ldy, N, D, ldy, w->b_out, b.yout, D, false, st)) != FLUX3_OK) return s;
 
@@ -1384,36 +1411,36 @@ flux3_status flux3_block_bwd(const flux3_dims* dims, const flux3_block_weights* 
     bwd_swiglu_kernel<<<(unsigned)(8 * sm_count()), 256, 0, st>>>(b.dycat, b.p, N, D, F, b.dp);
     prof_after(st);
     if ((s = launch_status()) != FLUX3_OK) return s;
-    // ---- attention, one head at a time with the score matrix in HBM
+    // ---- attention, one head at a time, keys as rows: P^T and dS^T come out of the GEMM
+    // epilogues (the forward pass's log2-sum-exp2 per query, rowsum(dO O) per query)
+    prof_before(FLUX3_KERNEL_BWD_ELEM, st);
+    attn_delta_kernel<<<(unsigned)(4 * sm_count()), 256, 0, st>>>(b.dycat, b.f.y, ldy, N, H, b.delta);
+    prof_after(st);
+    if ((s = launch_status()) != FLUX3_OK) return s;
+    const float sc_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
     for (int h = 0; h < H; ++h) {
         const __nv_bfloat16* qh = b.f.q + (size_t)h * N * 128;
         const __nv_bfloat16* kh = b.f.k + (size_t)h * N * 128;
         const __nv_bfloat16* doh = b.dycat + (size_t)h * 128;     // row stride ldy
-        const __nv_bfloat16* oh = b.f.y + (size_t)h * 128;        // row stride ldy
         const __nv_bfloat16* vh = b.p + 2 * D + (size_t)h * 128;  // row stride n_in
-        if ((s = run_gemm_plain(qh, 128, kh, 128, N, N, 128, nullptr, b.s, ldn, false, st)) != FLUX3_OK) return s;
-        prof_before(FLUX3_KERNEL_BWD_ELEM, st);
-        softmax_rows_kernel<<<(unsigned)N, 256, 0, st>>>(b.s, N, ldn, sc, b.pr, ldn);
-        prof_after(st);
-        if ((s = launch_status()) != FLUX3_OK) return s;
-        if ((s = run_transpose(b.pr, N, N, ldn, b.prT, ldn, st)) != FLUX3_OK) return s;
+        // P^T = exp2(scale_log2 k q^T - lse);  dV = P^T dO
+        if ((s = run_gemm_attn_t<EPI_PROB_T>(kh, 128, qh, 128, N, N, 128, b.lse + (size_t)h * N, nullptr, 0, sc_log2, b.pT,
+                                             ldn, st)) != FLUX3_OK)
+            return s;
         if ((s = run_transpose(doh, N, 128, ldy, b.doT, ldn, st)) != FLUX3_OK) return s;
-        // dV = P^T dO
-        if ((s = run_gemm_plain(b.prT, ldn, b.doT, ldn, N, 128, N, nullptr, b.dv + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+        if ((s = run_gemm_plain(b.pT, ldn, b.doT, ldn, N, 128, N, nullptr, b.dv + (size_t)h * 128, D, false, st)) != FLUX3_OK)
             return s;
-        // dP = dO V^T, then dS = scale P (dP - rowsum(dO O))
-        if ((s = run_gemm_plain(doh, ldy, vh, n_in, N, N, 128, nullptr, b.s, ldn, false, st)) != FLUX3_OK) return s;
-        prof_before(FLUX3_KERNEL_BWD_ELEM, st);
-        attn_ds_kernel<<<(unsigned)N, 256, 0, st>>>(b.s, ldn, b.pr, ldn, doh, ldy, oh, ldy, N, sc, b.ds, ldn);
-        prof_after(st);
-        if ((s = launch_status()) != FLUX3_OK) return s;
-        // dQ = dS K, dK = dS^T Q
-        if ((s = run_transpose(kh, N, 128, 128, b.kT, ldn, st)) != FLUX3_OK) return s;
-        if ((s = run_gemm_plain(b.ds, ldn, b.kT, ldn, N, 128, N, nullptr, b.dq + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+        // dS^T = scale P^T (v dO^T - delta);  dK = dS^T q
+        if ((s = run_gemm_attn_t<EPI_DS_T>(vh, n_in, doh, ldy, N, N, 128, b.delta + (size_t)h * N, b.pT, ldn, sc, b.dsT,
+                                           ldn, st)) != FLUX3_OK)
             return s;
-        if ((s = run_transpose(b.ds, N, N, ldn, b.prT, ldn, st)) != FLUX3_OK) return s;
         if ((s = run_transpose(qh, N, 128, 128, b.qT, ldn, st)) != FLUX3_OK) return s;
-        if ((s = run_gemm_plain(b.prT, ldn, b.qT, ldn, N, 128, N, nullptr, b.dk + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+        if ((s = run_gemm_plain(b.dsT, ldn, b.qT, ldn, N, 128, N, nullptr, b.dk + (size_t)h * 128, D, false, st)) != FLUX3_OK)
+            return s;
+        // dQ = dS k
+        if ((s = run_transpose(b.dsT, N, N, ldn, b.dsn, ldn, st)) != FLUX3_OK) return s;
+        if ((s = run_transpose(kh, N, 128, 128, b.kT, ldn, st)) != FLUX3_OK) return s;
+        if ((s = run_gemm_plain(b.dsn, ldn, b.kT, ldn, N, 128, N, nullptr, b.dq + (size_t)h * 128, D, false, st)) != FLUX3_OK)
             return s;
     }
     // ---- RoPE, QK RMSNorm and the V columns of dP; then P = a W_in^T + b_in

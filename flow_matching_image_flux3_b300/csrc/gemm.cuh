@@ -25,7 +25,7 @@ constexpr int GEMM_BK = 64;  // bf16 elements per 128-byte swizzle row
 // projections, whose shorter mainloop no longer hides a 4-warp epilogue).
 __host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 
-enum EpiKind { EPI_QKV_SWIGLU = 0, EPI_GATED_RESIDUAL = 1, EPI_F32 = 2, EPI_BF16 = 3 };
+enum EpiKind { EPI_QKV_SWIGLU = 0, EPI_GATED_RESIDUAL = 1, EPI_F32 = 2, EPI_BF16 = 3, EPI_PROB_T = 4, EPI_DS_T = 5 };
 
 struct GemmGroup {
     int row_begin, row_end, tile_begin, wset;
@@ -64,6 +64,11 @@ struct GemmParams {
     __nv_bfloat16* out_bf;
     int ld_out;
     int n_cols;  // columns of the output: a tile's columns at or past it are not stored
+    // EPI_PROB_T / EPI_DS_T (attention backward, keys as rows and queries as columns)
+    const float* col_vec;        // per column: the query's log2-sum-exp2 / its rowsum(dO O)
+    const __nv_bfloat16* aux;    // EPI_DS_T: the probabilities P^T, row stride ld_aux
+    int ld_aux;
+    float alpha;                 // EPI_PROB_T: log2(e) / sqrt(d);  EPI_DS_T: 1 / sqrt(d)
 };
 
 template <int BN>
@@ -339,6 +344,53 @@ F3_DEV void epi_bf16(const GemmParams& p, const EpiWeights& w, int n, uint32_t t
     }
 }
 
+// Attention backward with keys as rows and queries as columns.  EPI_PROB_T: the
+// accumulator is k q^T; P^T = exp2(alpha acc - lse[query]) in bf16.  EPI_DS_T: the
+// accumulator is v dO^T = dP^T; dS^T = alpha P^T (acc - delta[query]) in bf16.
+template <int BN, int EPI>
+F3_DEV void epi_attn_t(const GemmParams& p, int n, uint32_t tacc, int r, bool valid) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t t[32];
+        tmem_ld32(tacc + c * 32, t);
+        tmem_ld_wait();
+        const int col = n * BN + c * 32;
+        if (!valid || col >= p.n_cols) continue;
+        float a[32];
+        unpack32(t, a);
+        const int lim = p.n_cols - col < 32 ? p.n_cols - col : 32;
+        if (EPI == EPI_PROB_T) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = i < lim ? exp2f(p.alpha * a[i] - __ldg(p.col_vec + col + i)) : 0.f;
+        } else {
+            const uint4* pa = reinterpret_cast<const uint4*>(p.aux + (size_t)r * p.ld_aux + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 u = v * 8 < lim ? pa[v] : make_uint4(0, 0, 0, 0);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 8 * v + 2 * e;
+                    const float p0 = __uint_as_float(w4[e] << 16), p1 = __uint_as_float(w4[e] & 0xffff0000u);
+                    a[i] = i < lim ? p.alpha * p0 * (a[i] - __ldg(p.col_vec + col + i)) : 0.f;
+                    a[i + 1] = i + 1 < lim ? p.alpha * p1 * (a[i + 1] - __ldg(p.col_vec + col + i + 1)) : 0.f;
+                }
+            }
+        }
+        __nv_bfloat16* dst = p.out_bf + (size_t)r * p.ld_out + col;
+        if (lim == 32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                st_global_v4(dst + 8 * i, pack_bf16(a[8 * i], a[8 * i + 1]), pack_bf16(a[8 * i + 2], a[8 * i + 3]),
+                             pack_bf16(a[8 * i + 4], a[8 * i + 5]), pack_bf16(a[8 * i + 6], a[8 * i + 7]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < lim) dst[i] = __float2bfloat16_rn(a[i]);
+        }
+    }
+}
+
 // --------------------------------------------------------------------- the kernel
 // Tiles are numbered n-major (all m-tiles of one weight tile run together, so each weight
 // tile is read from HBM once).  With CL = 2 the kernel runs as clusters of two CTAs that
@@ -521,7 +573,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_tcgen05_kernel(const
             if (EPI == EPI_QKV_SWIGLU) epi_qkv<AK, EW / 4>(p, w, ti.n, tacc, valid ? r : 0, valid, part);
             else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN, AK>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_F32) epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
-            else epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else if (EPI == EPI_BF16) epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
+            else epi_attn_t<BN, EPI>(p, ti.n, tacc, valid ? r : 0, valid);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
