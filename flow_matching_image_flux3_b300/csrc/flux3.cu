@@ -627,7 +627,7 @@ flux3_status run_gemm_attn_t(const void* A, int lda, const void* B, int ldb, int
     P.aux = static_cast<const __nv_bfloat16*>(aux);
     P.ld_aux = ld_aux;
     P.alpha = alpha;
-    return launch_gemm<256, EPI, 1>(P, st, FLUX3_KERNEL_BWD_GEMM);
+    return launch_gemm<256, EPI, 1, 0, 8>(P, st, FLUX3_KERNEL_BWD_GEMM);
 }
 
 // dst [cols, ld_dst] = src [rows, cols]^T (bf16)

@@ -347,10 +347,10 @@ F3_DEV void epi_bf16(const GemmParams& p, const EpiWeights& w, int n, uint32_t t
 // Attention backward with keys as rows and queries as columns.  EPI_PROB_T: the
 // accumulator is k q^T; P^T = exp2(alpha acc - lse[query]) in bf16.  EPI_DS_T: the
 // accumulator is v dO^T = dP^T; dS^T = alpha P^T (acc - delta[query]) in bf16.
-template <int BN, int EPI>
-F3_DEV void epi_attn_t(const GemmParams& p, int n, uint32_t tacc, int r, bool valid) {
+template <int BN, int EPI, int NPARTS>
+F3_DEV void epi_attn_t(const GemmParams& p, int n, uint32_t tacc, int r, bool valid, int part) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = part; c < BN / 32; c += NPARTS) {
         uint32_t t[32];
         tmem_ld32(tacc + c * 32, t);
         tmem_ld_wait();
@@ -424,7 +424,8 @@ template <int BN, int EPI, int CL, int AK = 0, int EW = 4>
 __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
     static_assert(CL == 1 || (CL == 2 && BN == 256), "clusters of two split a 256-row B tile");
     static_assert(AK == 0 || EPI == EPI_QKV_SWIGLU || EPI == EPI_GATED_RESIDUAL, "e4m3 operands: the projections");
-    static_assert(EW == 4 || (EW == 8 && EPI == EPI_QKV_SWIGLU), "8 epilogue warps: input projection only");
+    static_assert(EW == 4 || (EW == 8 && (EPI == EPI_QKV_SWIGLU || EPI == EPI_PROB_T || EPI == EPI_DS_T)),
+                  "8 epilogue warps: the input projection and the attention-backward epilogues");
     constexpr int KB_ELEMS = AK ? 128 : GEMM_BK;
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1) gemm_tcgen05_kernel(const
             else if (EPI == EPI_GATED_RESIDUAL) epi_gated_residual<BN, AK>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_F32) epi_f32<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
             else if (EPI == EPI_BF16) epi_bf16<BN>(p, w, ti.n, tacc, valid ? r : 0, valid);
-            else epi_attn_t<BN, EPI>(p, ti.n, tacc, valid ? r : 0, valid);
+            else epi_attn_t<BN, EPI, EW / 4>(p, ti.n, tacc, valid ? r : 0, valid, part);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
