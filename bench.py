@@ -73,8 +73,8 @@ def block_flops(D, F, n):
 # DRAM traffic of one in_proj launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
 # ncu capture summarised in profiles/joint_block_4256_ncu_full.md; reported only while the
 # kernel sources are the ones that capture measured.
-IN_PROJ_TRAFFIC_BYTES = (201.138432 + 140.202240) * 1e6
-IN_PROJ_SOURCES = {"gemm.cuh": "b2571096384aaa0a", "sm103.cuh": "86ccb8d589deb628", "flux3.cu": "a9964237d87c6d29"}
+IN_PROJ_TRAFFIC_BYTES = (201.990912 + 140.658688) * 1e6
+IN_PROJ_SOURCES = {"gemm.cuh": "47b19e260ee46ab8", "sm103.cuh": "86ccb8d589deb628", "flux3.cu": "c33c243ff17041b7"}
 
 
 def in_proj_traffic():

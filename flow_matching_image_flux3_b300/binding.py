@@ -111,6 +111,9 @@ def _load() -> ctypes.CDLL:
         "flux3_block_bwd_workspace_size": (c_size, [P(flux3_dims), c_i32]),
         "flux3_block_bwd": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp, c_vp, c_i32,
                                     c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+        "flux3_stream_block_bwd_workspace_size": (c_size, [P(flux3_dims), P(flux3_segments)]),
+        "flux3_stream_block_bwd": (c_i32, [P(flux3_dims), P(flux3_block_weights), P(flux3_segments), c_vp, c_vp, c_vp,
+                                           c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
         "flux3_nvfp4_scale_bytes": (c_size, [c_i32, c_i32]),
         "flux3_quantize_rows_nvfp4": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
         "flux3_in_proj_nvfp4_fwd": (c_i32, [P(flux3_dims), P(flux3_block_weights_nvfp4), c_vp, c_vp, c_vp, c_i32, c_vp,
@@ -142,7 +145,8 @@ EXPORTED = [
     "flux3_sample_fwd", "flux3_quantize_rows_fp8", "flux3_in_proj_fp8_fwd", "flux3_block_fp8_workspace_size",
     "flux3_block_fp8_fwd", "flux3_selftest_timeout", "flux3_nvfp4_scale_bytes", "flux3_quantize_rows_nvfp4",
     "flux3_in_proj_nvfp4_fwd", "flux3_block_nvfp4_workspace_size", "flux3_block_nvfp4_fwd",
-    "flux3_block_bwd_workspace_size", "flux3_block_bwd",
+    "flux3_block_bwd_workspace_size", "flux3_block_bwd", "flux3_stream_block_bwd_workspace_size",
+    "flux3_stream_block_bwd",
 ]
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -542,6 +546,29 @@ def block_bwd(dims, weights, seg_off: Sequence[int], mod: torch.Tensor, x: torch
                                                   _ptr(dxo, torch.float32), n, f("dx"), f("dw_in"), f("db_in"),
                                                   f("dq_norm"), f("dk_norm"), f("dw_out"), f("db_out"), f("dmod"),
                                                   _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def stream_block_bwd(dims, weights: Sequence, seg_off: Sequence[int], mod: torch.Tensor, x: torch.Tensor,
+                     rope: torch.Tensor, dxo: torch.Tensor, stream=None) -> dict:
+    """Gradients of the stage-1 block (flux3_stream_block_bwd): dx [N, D] and, per stream,
+    dw_in, db_in, dq_norm, dk_norm, dw_out, db_out, dmod stacked along a leading axis."""
+    n, D = x.shape
+    F = dims.ffn_hidden
+    g = len(seg_off) - 1
+    dev = x.device
+    out = {"dx": torch.empty(n, D, device=dev), "dw_in": torch.empty(g, 3 * D + 2 * F, D, device=dev),
+           "db_in": torch.empty(g, 3 * D + 2 * F, device=dev), "dq_norm": torch.empty(g, 128, device=dev),
+           "dk_norm": torch.empty(g, 128, device=dev), "dw_out": torch.empty(g, D, D + F, device=dev),
+           "db_out": torch.empty(g, D, device=dev), "dmod": torch.empty(g, 3, D, device=dev)}
+    d, s = make_dims(dims), Segments(seg_off, mod)
+    ws = workspace(int(lib.flux3_stream_block_bwd_workspace_size(ctypes.byref(d), ctypes.byref(s.s))), dev)
+    wa = _weights_array(weights)
+    f = lambda k: _ptr(out[k], torch.float32)
+    _check("flux3_stream_block_bwd", lib.flux3_stream_block_bwd(
+        ctypes.byref(d), wa, ctypes.byref(s.s), _ptr(x, torch.bfloat16), _ptr(rope, torch.float32),
+        _ptr(dxo, torch.float32), n, f("dx"), f("dw_in"), f("db_in"), f("dq_norm"), f("dk_norm"), f("dw_out"),
+        f("db_out"), f("dmod"), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

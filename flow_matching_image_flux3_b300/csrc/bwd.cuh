@@ -15,20 +15,46 @@ namespace f3 {
 
 constexpr int BWD_ROWS = 32;  // rows per CTA of the column-sum kernels
 
-// dst[c][r] = src[r][c] for a bf16 [rows, cols] matrix (row strides in elements); 32 x 32
-// tiles through shared memory, block (32, 8).
-__global__ void transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int rows, int cols, int ld_src,
-                                      __nv_bfloat16* __restrict__ dst, int ld_dst) {
-    __shared__ __nv_bfloat16 tile[32][34];
-    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-    for (int i = threadIdx.y; i < 32; i += 8) {
-        const int r = r0 + i, c = c0 + threadIdx.x;
-        if (r < rows && c < cols) tile[i][threadIdx.x] = src[(size_t)r * ld_src + c];
+// dst[c][r] = src[r][c] for a bf16 [rows, cols] matrix (row strides in elements, even,
+// both bases 4-byte aligned): 64 x 64 tiles through shared memory, block (32, 8), each
+// thread reading two adjacent columns and writing two adjacent rows (bf16 pairs); a ragged
+// edge falls back to single elements.  The tile's row stride of 65 keeps both phases free
+// of bank conflicts.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int rows, int cols,
+                                                            int ld_src, __nv_bfloat16* __restrict__ dst, int ld_dst) {
+    __shared__ __nv_bfloat16 tile[64][65];
+    const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+    const int c = c0 + 2 * threadIdx.x;
+    for (int i = threadIdx.y; i < 64; i += 8) {
+        const int r = r0 + i;
+        __nv_bfloat16 e0 = __float2bfloat16_rn(0.f), e1 = e0;
+        if (r < rows) {
+            const __nv_bfloat16* sp = src + (size_t)r * ld_src + c;
+            if (c + 1 < cols) {
+                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(sp);
+                e0 = v.x;
+                e1 = v.y;
+            } else if (c < cols) {
+                e0 = sp[0];
+            }
+        }
+        tile[i][2 * threadIdx.x] = e0;
+        tile[i][2 * threadIdx.x + 1] = e1;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += 8) {
-        const int c = c0 + i, r = r0 + threadIdx.x;
-        if (c < cols && r < rows) dst[(size_t)c * ld_dst + r] = tile[threadIdx.x][i];
+    const int r = r0 + 2 * threadIdx.x;
+    for (int i = threadIdx.y; i < 64; i += 8) {
+        const int cc = c0 + i;
+        if (cc >= cols) continue;
+        __nv_bfloat16* dp = dst + (size_t)cc * ld_dst + r;
+        if (r + 1 < rows) {
+            __nv_bfloat162 v;
+            v.x = tile[2 * threadIdx.x][i];
+            v.y = tile[2 * threadIdx.x + 1][i];
+            *reinterpret_cast<__nv_bfloat162*>(dp) = v;
+        } else if (r < rows) {
+            dp[0] = tile[2 * threadIdx.x][i];
+        }
     }
 }
 

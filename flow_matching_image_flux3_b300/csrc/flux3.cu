@@ -630,11 +630,13 @@ flux3_status run_gemm_attn_t(const void* A, int lda, const void* B, int ldb, int
     return launch_gemm<256, EPI, 1, 0, 8>(P, st, FLUX3_KERNEL_BWD_GEMM);
 }
 
-// dst [cols, ld_dst] = src [rows, cols]^T (bf16)
+// dst [cols, ld_dst] = src [rows, cols]^T (bf16; even strides, 4-byte aligned bases)
 flux3_status run_transpose(const void* src, int rows, int cols, int ld_src, void* dst, int ld_dst, cudaStream_t st) {
     if (rows == 0 || cols == 0) return FLUX3_OK;
+    if ((ld_src | ld_dst) & 1 || (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 3)
+        return FLUX3_ERR_INVALID_ARG;
     prof_before(FLUX3_KERNEL_BWD_ELEM, st);
-    transpose_bf16_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32)), dim3(32, 8), 0, st>>>(
+    transpose_bf16_kernel<<<dim3((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64)), dim3(32, 8), 0, st>>>(
         static_cast<const __nv_bfloat16*>(src), rows, cols, ld_src, static_cast<__nv_bfloat16*>(dst), ld_dst);
     prof_after(st);
     return launch_status();
@@ -1471,6 +1473,58 @@ flux3_status flux3_block_bwd(const flux3_dims* dims, const flux3_block_weights* 
         b.da, static_cast<const __nv_bfloat16*>(x), b.stats, N, D, so, dmod);
     prof_after(st);
     return launch_status();
+}
+
+size_t flux3_stream_block_bwd_workspace_size(const flux3_dims* dims, const flux3_segments* segs) {
+    if (check_dims(dims) != FLUX3_OK || !segs || segs->n_seg < 1 || segs->n_seg > FLUX3_MAX_SEGMENTS || !segs->seg_off)
+        return 0;
+    size_t need = 0;
+    for (int s = 0; s < segs->n_seg; ++s) {
+        const int n = segs->seg_off[s + 1] - segs->seg_off[s];
+        if (n < 0 || n > kMaxTokens) return 0;
+        const size_t b = flux3_block_bwd_workspace_size(dims, n);
+        need = b > need ? b : need;
+    }
+    return need;
+}
+
+flux3_status flux3_stream_block_bwd(const flux3_dims* dims, const flux3_block_weights* w, const flux3_segments* segs,
+                                    const void* x, const float* rope, const float* dxo, int32_t n_tokens, float* dx,
+                                    float* dw_in, float* db_in, float* dq_norm, float* dk_norm, float* dw_out,
+                                    float* db_out, float* dmod, void* ws, size_t ws_bytes, flux3_stream_t stream) {
+    flux3_status s = check_dims(dims);
+    if (s != FLUX3_OK) return s;
+    if (n_tokens < 0 || n_tokens > kMaxTokens) return FLUX3_ERR_INVALID_ARG;
+    if ((s = check_segs(segs, n_tokens, true)) != FLUX3_OK) return s;
+    if ((s = check_weights(w, segs->n_seg, true, true)) != FLUX3_OK) return s;
+    if (n_tokens == 0) return FLUX3_OK;
+    if (!ws || ws_bytes < flux3_stream_block_bwd_workspace_size(dims, segs)) return FLUX3_ERR_WORKSPACE;
+    const size_t D = dims->width, F = dims->ffn_hidden, n_in = 3 * D + 2 * F;
+    // stage 1: every stream runs its own block on its own rows and attends only to itself,
+    // so the block's backward is the joint block's backward of each stream on its own
+    for (int g = 0; g < segs->n_seg; ++g) {
+        const int lo = segs->seg_off[g], n = segs->seg_off[g + 1] - lo;
+        if (n == 0) {  // an empty stream: its parameters get zero gradients
+            cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+            if (cudaMemsetAsync(dw_in + g * n_in * D, 0, n_in * D * 4, st) != cudaSuccess ||
+                cudaMemsetAsync(db_in + g * n_in, 0, n_in * 4, st) != cudaSuccess ||
+                cudaMemsetAsync(dq_norm + g * 128, 0, 128 * 4, st) != cudaSuccess ||
+                cudaMemsetAsync(dk_norm + g * 128, 0, 128 * 4, st) != cudaSuccess ||
+                cudaMemsetAsync(dw_out + g * D * (D + F), 0, D * (D + F) * 4, st) != cudaSuccess ||
+                cudaMemsetAsync(db_out + g * D, 0, D * 4, st) != cudaSuccess ||
+                cudaMemsetAsync(dmod + g * 3 * D, 0, 3 * D * 4, st) != cudaSuccess)
+                return FLUX3_ERR_CUDA;
+            continue;
+        }
+        const int32_t one[2] = {0, n};
+        const flux3_segments sg{1, one, segs->mod + g * 3 * D};
+        s = flux3_block_bwd(dims, w + g, &sg, static_cast<const __nv_bfloat16*>(x) + (size_t)lo * D, rope + (size_t)lo * 128,
+                            dxo + (size_t)lo * D, n, dx + (size_t)lo * D, dw_in + g * n_in * D, db_in + g * n_in,
+                            dq_norm + g * 128, dk_norm + g * 128, dw_out + g * D * (D + F), db_out + g * D, dmod + g * 3 * D,
+                            ws, ws_bytes, stream);
+        if (s != FLUX3_OK) return s;
+    }
+    return FLUX3_OK;
 }
 
 flux3_status flux3_device_error(uint32_t* flags, int32_t reset) {

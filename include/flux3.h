@@ -446,6 +446,19 @@ flux3_status flux3_block_bwd(const flux3_dims *dims, const flux3_block_weights *
                              float *dw_in, float *db_in, float *dq_norm, float *dk_norm, float *dw_out, float *db_out,
                              float *dmod, void *ws, size_t ws_bytes, flux3_stream_t stream);
 
+/* The stage-1 (per-stream) block's backward: stream s has its own weights w[s] and
+ * attends only to itself ("How it works", stage 1), so its gradients are those of the joint
+ * block run on that stream alone.  Arguments as flux3_block_bwd with w [n_seg] and the
+ * parameter gradients one set per stream, concatenated: dw_in [n_seg][3D + 2F][D],
+ * db_in [n_seg][3D + 2F], dq_norm and dk_norm [n_seg][128], dw_out [n_seg][D][D + F],
+ * db_out [n_seg][D], dmod [n_seg][3][D]; an empty stream gets zero gradients.  Workspace
+ * flux3_stream_block_bwd_workspace_size bytes (that of the longest stream). */
+size_t flux3_stream_block_bwd_workspace_size(const flux3_dims *dims, const flux3_segments *segs);
+flux3_status flux3_stream_block_bwd(const flux3_dims *dims, const flux3_block_weights *w, const flux3_segments *segs,
+                                    const void *x, const float *rope, const float *dxo, int32_t n_tokens, float *dx,
+                                    float *dw_in, float *db_in, float *dq_norm, float *dk_norm, float *dw_out,
+                                    float *db_out, float *dmod, void *ws, size_t ws_bytes, flux3_stream_t stream);
+
 /* ---- flux3_block_fwd without a caller-provided workspace.
  * This entry point has no counterpart in the model description; it is a service for
  * callers that cannot allocate device memory: for example a host program that hands all

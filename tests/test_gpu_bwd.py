@@ -72,3 +72,28 @@ def test_block_backward_full_size():
     print(errs)
     for k in KEYS:
         assert errs[k] <= GRAD_REL_L2, (k, errs[k])
+
+
+def test_stream_block_backward_stage1():
+    """The stage-1 block (a weight set per stream, attention inside each stream): every
+    stream's gradients against the backward oracle run on that stream alone, dx on all rows."""
+    streams = [synth.Stream("image", 130, (10, 13)), synth.text_stream(160), synth.Stream("ref", 35, (5, 7), t=1)]
+    case = synth.make_case(synth.TINY, streams, seed=54, stage=1, bias=True)
+    d = case.dims
+    dxo = torch.randn(case.n, d.width, generator=torch.Generator("cpu").manual_seed(55))
+    ws = [DevWeights(w) for w in case.weights]
+    rope = B.rope_build(d, case.pos.cuda())
+    got = B.stream_block_bwd(d, ws, case.seg_off, case.mod.cuda(), case.x.cuda(), rope, dxo.cuda())
+    torch.cuda.synchronize()
+    ang = O.rope_angles(case.pos.numpy(), d.rope_theta)
+    x64, mod64 = synth.as_f64(case.x), synth.as_f64(case.mod)
+    dx_ref = np.empty(x64.shape)
+    for g in range(len(case.seg_off) - 1):
+        lo, hi = case.seg_off[g], case.seg_off[g + 1]
+        ref = block_backward(x64[lo:hi], oracle_weights(case.weights[g]), [0, hi - lo], mod64[g:g + 1], ang[lo:hi],
+                             d.heads, dxo[lo:hi].double().numpy(), ln_eps=d.ln_eps, rms_eps=d.rms_eps)
+        dx_ref[lo:hi] = ref["dx"]
+        for k in KEYS[1:]:
+            e = rel_l2(f64(got[k][g]), ref[k] if k != "dmod" else ref[k][0])
+            assert e <= GRAD_REL_L2, (g, k, e)
+    assert rel_l2(f64(got["dx"]), dx_ref) <= GRAD_REL_L2
