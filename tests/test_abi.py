@@ -173,3 +173,33 @@ def test_nvfp4_argument_checks(B):
                                          FAKE16, FAKE16, FAKE16, 96, FAKE16, None) == B.ERR_INVALID_ARG   # ld_vt < N
     assert B.lib.flux3_block_nvfp4_workspace_size(ctypes.byref(d), 144) > B.lib.flux3_block_workspace_size(
         ctypes.byref(d), 144)
+
+
+def test_backward_argument_checks(B):
+    d = _dims(B)
+    off = (ctypes.c_int32 * 3)(0, 64, 144)
+    segs = B.flux3_segments(2, ctypes.cast(off, ctypes.POINTER(ctypes.c_int32)), FAKE)
+    w = B.flux3_block_weights(FAKE, None, FAKE, FAKE, FAKE, None)
+    outs = [FAKE] * 8
+    assert B.lib.flux3_block_bwd_workspace_size(ctypes.byref(d), 144) > B.lib.flux3_block_workspace_size(
+        ctypes.byref(d), 144)
+    # no workspace
+    assert B.lib.flux3_block_bwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(segs), FAKE, FAKE, FAKE, 144, *outs,
+                                 None, 0, None) == B.ERR_WORKSPACE
+    # a missing output
+    assert B.lib.flux3_block_bwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(segs), FAKE, FAKE, FAKE, 144,
+                                 *([None] + outs[1:]), FAKE, 1 << 40, None) == B.ERR_INVALID_ARG
+    # segments that do not end at N
+    assert B.lib.flux3_block_bwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(segs), FAKE, FAKE, FAKE, 150, *outs,
+                                 FAKE, 1 << 40, None) == B.ERR_INVALID_ARG
+    # nothing to do
+    e = (ctypes.c_int32 * 2)(0, 0)
+    s0 = B.flux3_segments(1, ctypes.cast(e, ctypes.POINTER(ctypes.c_int32)), FAKE)
+    assert B.lib.flux3_block_bwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(s0), None, None, None, 0,
+                                 *([None] * 8), None, 0, None) == B.OK
+    # the per-stream form needs a weight set per stream and the longest stream's workspace
+    assert B.lib.flux3_stream_block_bwd_workspace_size(ctypes.byref(d), ctypes.byref(segs)) == \
+        B.lib.flux3_block_bwd_workspace_size(ctypes.byref(d), 80)
+    ws2 = (B.flux3_block_weights * 2)(w, B.flux3_block_weights(None, None, FAKE, FAKE, FAKE, None))
+    assert B.lib.flux3_stream_block_bwd(ctypes.byref(d), ws2, ctypes.byref(segs), FAKE, FAKE, FAKE, 144, *outs, FAKE,
+                                        1 << 40, None) == B.ERR_INVALID_ARG
