@@ -19,6 +19,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -108,7 +109,10 @@ class Clocks:
         self.index = index
         self.proc = None
         self.t0 = self.t1 = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples go to FLUX3_CLOCKS_DIR if set, else to the system's temp directory;
+        # the JSON line carries their summary
+        out_dir = os.environ.get("FLUX3_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"flux3_clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
