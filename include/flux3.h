@@ -12,7 +12,8 @@
  * tokens only.  The QK normalisation with a learned scale follows the module names
  * "*.{query,key}_norm.scale" on the Miles page "FLUX 3 Image Klein", section 3
  * ("Family config"), and the absence of a padding mask follows the same table
- * (row "Micro-batch") and "How it works" (the transformer attends to the padding).
+ * (row "Micro-batch") and "How it works" (the text is padded to a multiple of 80 tokens
+ * and the padded tokens are attended, not masked).
  *
  * Conventions for every entry point
  *  - The caller owns all memory.  Pointers marked "device" must point to device
