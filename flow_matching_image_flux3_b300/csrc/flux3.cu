@@ -1303,9 +1303,11 @@ flux3_status flux3_block_nvfp4_fwd(const flux3_dims* dims, const flux3_block_wei
 
 // ---------------------------------------------------------------- the joint block's backward
 namespace {
+constexpr int kBwdSlots = 4;  // heads whose attention backward runs concurrently
 struct BwdWs {
     BlockWs f;                      // the forward pass recomputed: a, q, k, V^T, [O | act]
-    __nv_bfloat16 *p, *dy, *dyT, *woT, *wiT, *dycat, *ycatT, *pT, *dsT, *dsn, *doT, *kT, *qT, *dp, *dpT, *aT;
+    __nv_bfloat16 *p, *dy, *dyT, *woT, *wiT, *dycat, *ycatT, *dp, *dpT, *aT;
+    __nv_bfloat16 *pT[kBwdSlots], *dsT[kBwdSlots], *dsn[kBwdSlots], *doT[kBwdSlots], *kT[kBwdSlots], *qT[kBwdSlots];
     float *yout, *lse, *delta, *dq, *dk, *dv, *da;
     float2* stats;
     int ldn;  // row stride of the [., N] buffers (N rounded up to 8)
@@ -1335,12 +1337,14 @@ BwdWs bwd_ws_layout(const flux3_dims* d, int N, uint8_t* base) {
     w.ycatT = bf((D + F) * ldn);
     w.lse = f32((size_t)d->heads * N);
     w.delta = f32((size_t)d->heads * N);
-    w.pT = bf((size_t)N * ldn);
-    w.dsT = bf((size_t)N * ldn);
-    w.dsn = bf((size_t)N * ldn);
-    w.doT = bf(128 * ldn);
-    w.kT = bf(128 * ldn);
-    w.qT = bf(128 * ldn);
+    for (int i = 0; i < kBwdSlots; ++i) {
+        w.pT[i] = bf((size_t)N * ldn);
+        w.dsT[i] = bf((size_t)N * ldn);
+        w.dsn[i] = bf((size_t)N * ldn);
+        w.doT[i] = bf(128 * ldn);
+        w.kT[i] = bf(128 * ldn);
+        w.qT[i] = bf(128 * ldn);
+    }
     w.dq = f32((size_t)N * D);
     w.dk = f32((size_t)N * D);
     w.dv = f32((size_t)N * D);
@@ -1351,6 +1355,23 @@ BwdWs bwd_ws_layout(const flux3_dims* d, int N, uint8_t* base) {
     w.stats = reinterpret_cast<float2*>(take((size_t)N * 8));
     w.bytes = off;
     return w;
+}
+}  // namespace
+
+namespace {
+// Library-owned streams of the current device on which the attention backward runs
+// several heads at once (created once per device, non-blocking).
+bool bwd_streams(cudaStream_t (&out)[kBwdSlots]) {
+    static std::mutex mu;
+    static cudaStream_t pool[64][kBwdSlots] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < kBwdSlots; ++i) {
+        if (!pool[dev][i] && cudaStreamCreateWithFlags(&pool[dev][i], cudaStreamNonBlocking) != cudaSuccess) return false;
+        out[i] = pool[dev][i];
+    }
+    return true;
 }
 }  // namespace
 
@@ -1420,31 +1441,61 @@ flux3_status flux3_block_bwd(const flux3_dims* dims, const flux3_block_weights* 
     prof_after(st);
     if ((s = launch_status()) != FLUX3_OK) return s;
     const float sc_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
-    for (int h = 0; h < H; ++h) {
+    // the heads run kBwdSlots at a time on library-owned streams forked from `st` and
+    // joined back into it by events (each head writes its own columns of dQ, dK, dV)
+    cudaStream_t hs[kBwdSlots];
+    if (!bwd_streams(hs)) return FLUX3_ERR_CUDA;
+    cudaEvent_t fork = nullptr, join[kBwdSlots] = {};
+    auto release = [&]() {
+        if (fork) cudaEventDestroy(fork);
+        for (int i = 0; i < kBwdSlots; ++i)
+            if (join[i]) cudaEventDestroy(join[i]);
+    };
+    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess || cudaEventRecord(fork, st) != cudaSuccess) {
+        release();
+        return FLUX3_ERR_CUDA;
+    }
+    for (int i = 0; i < kBwdSlots; ++i)
+        if (cudaEventCreateWithFlags(&join[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaStreamWaitEvent(hs[i], fork, 0) != cudaSuccess) {
+            release();
+            return FLUX3_ERR_CUDA;
+        }
+    for (int h = 0; h < H && s == FLUX3_OK; ++h) {
+        const int sl = h % kBwdSlots;
+        cudaStream_t hst = hs[sl];
         const __nv_bfloat16* qh = b.f.q + (size_t)h * N * 128;
         const __nv_bfloat16* kh = b.f.k + (size_t)h * N * 128;
         const __nv_bfloat16* doh = b.dycat + (size_t)h * 128;     // row stride ldy
         const __nv_bfloat16* vh = b.p + 2 * D + (size_t)h * 128;  // row stride n_in
         // P^T = exp2(scale_log2 k q^T - lse);  dV = P^T dO
-        if ((s = run_gemm_attn_t<EPI_PROB_T>(kh, 128, qh, 128, N, N, 128, b.lse + (size_t)h * N, nullptr, 0, sc_log2, b.pT,
-                                             ldn, st)) != FLUX3_OK)
-            return s;
-        if ((s = run_transpose(doh, N, 128, ldy, b.doT, ldn, st)) != FLUX3_OK) return s;
-        if ((s = run_gemm_plain(b.pT, ldn, b.doT, ldn, N, 128, N, nullptr, b.dv + (size_t)h * 128, D, false, st)) != FLUX3_OK)
-            return s;
+        if ((s = run_gemm_attn_t<EPI_PROB_T>(kh, 128, qh, 128, N, N, 128, b.lse + (size_t)h * N, nullptr, 0, sc_log2,
+                                             b.pT[sl], ldn, hst)) != FLUX3_OK ||
+            (s = run_transpose(doh, N, 128, ldy, b.doT[sl], ldn, hst)) != FLUX3_OK ||
+            (s = run_gemm_plain(b.pT[sl], ldn, b.doT[sl], ldn, N, 128, N, nullptr, b.dv + (size_t)h * 128, D, false, hst)) !=
+                FLUX3_OK)
+            break;
         // dS^T = scale P^T (v dO^T - delta);  dK = dS^T q
-        if ((s = run_gemm_attn_t<EPI_DS_T>(vh, n_in, doh, ldy, N, N, 128, b.delta + (size_t)h * N, b.pT, ldn, sc, b.dsT,
-                                           ldn, st)) != FLUX3_OK)
-            return s;
-        if ((s = run_transpose(qh, N, 128, 128, b.qT, ldn, st)) != FLUX3_OK) return s;
-        if ((s = run_gemm_plain(b.dsT, ldn, b.qT, ldn, N, 128, N, nullptr, b.dk + (size_t)h * 128, D, false, st)) != FLUX3_OK)
-            return s;
+        if ((s = run_gemm_attn_t<EPI_DS_T>(vh, n_in, doh, ldy, N, N, 128, b.delta + (size_t)h * N, b.pT[sl], ldn, sc,
+                                           b.dsT[sl], ldn, hst)) != FLUX3_OK ||
+            (s = run_transpose(qh, N, 128, 128, b.qT[sl], ldn, hst)) != FLUX3_OK ||
+            (s = run_gemm_plain(b.dsT[sl], ldn, b.qT[sl], ldn, N, 128, N, nullptr, b.dk + (size_t)h * 128, D, false, hst)) !=
+                FLUX3_OK)
+            break;
         // dQ = dS k
-        if ((s = run_transpose(b.dsT, N, N, ldn, b.dsn, ldn, st)) != FLUX3_OK) return s;
-        if ((s = run_transpose(kh, N, 128, 128, b.kT, ldn, st)) != FLUX3_OK) return s;
-        if ((s = run_gemm_plain(b.dsn, ldn, b.kT, ldn, N, 128, N, nullptr, b.dq + (size_t)h * 128, D, false, st)) != FLUX3_OK)
-            return s;
+        if ((s = run_transpose(b.dsT[sl], N, N, ldn, b.dsn[sl], ldn, hst)) != FLUX3_OK ||
+            (s = run_transpose(kh, N, 128, 128, b.kT[sl], ldn, hst)) != FLUX3_OK ||
+            (s = run_gemm_plain(b.dsn[sl], ldn, b.kT[sl], ldn, N, 128, N, nullptr, b.dq + (size_t)h * 128, D, false, hst)) !=
+                FLUX3_OK)
+            break;
     }
+    for (int i = 0; i < kBwdSlots; ++i)
+        if (cudaEventRecord(join[i], hs[i]) != cudaSuccess || cudaStreamWaitEvent(st, join[i], 0) != cudaSuccess) {
+            release();
+            return FLUX3_ERR_CUDA;
+        }
+    release();
+    if (s != FLUX3_OK) return s;
     // ---- RoPE, QK RMSNorm and the V columns of dP; then P = a W_in^T + b_in
     prof_before(FLUX3_KERNEL_BWD_ELEM, st);
     bwd_qk_kernel<<<(unsigned)(4 * sm_count()), 256, 0, st>>>(b.dq, b.dk, b.dv, b.p, reinterpret_cast<const float2*>(rope),

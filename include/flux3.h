@@ -440,7 +440,10 @@ flux3_status flux3_block_nvfp4_fwd(const flux3_dims *dims, const flux3_block_wei
  * probability matrices are materialized in the workspace one head at a time.  Arguments x,
  * rope, segs, w as flux3_block_fwd (w's biases may be NULL: their gradients are still
  * written); dxo fp32 [N, D].  All outputs are overwritten; workspace
- * flux3_block_bwd_workspace_size bytes (about 1.6 GB at N = 4,256 and width 3072). */
+ * flux3_block_bwd_workspace_size bytes (about 2.2 GB at N = 4,256 and width 3072).
+ * Attention's backward runs four heads at a time on four library-owned streams of the
+ * current device, forked from `stream` and joined back into it with events (so the call
+ * stays asynchronous and capturable into a CUDA graph). */
 size_t flux3_block_bwd_workspace_size(const flux3_dims *dims, int32_t n_tokens);
 flux3_status flux3_block_bwd(const flux3_dims *dims, const flux3_block_weights *w, const flux3_segments *segs,
                              const void *x, const float *rope, const float *dxo, int32_t n_tokens, float *dx,
